@@ -1,0 +1,175 @@
+"""CPU oracle for frame-aligned window-sparse attention.
+
+TEST INFRASTRUCTURE ONLY.  Only tests/, __graft_entry__.smoke() and the
+cpu_baseline / reference legs of bench.py may import this package.  It shares
+no code with the CUDA library (frame_aligned_window_gb300) and never imports
+it; the only module both sides use is `workloads` (seeded inputs).
+
+`oracle.c` is plain fp64 C (built here with gcc and OpenMP); `brute.py` is a
+second, pure-Python restatement used to pin the C code on tiny inputs.
+
+Parity status: every function here is pinned by tests under tests/ against
+brute force, closed forms, invariants or a library routine (see the
+test_oracle_* files).  The pages' TPU figures (fraction of the TPU bound,
+share of eligible heads) are context only and not pinned.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import subprocess
+import threading
+
+import numpy as np
+import torch
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+_SRC = os.path.join(_HERE, "oracle.c")
+_BUILD = os.path.join(_HERE, "_build")
+_LIB_PATH = os.path.join(_BUILD, "liboracle.so")
+_lib = None
+_lock = threading.Lock()
+
+# tau of the fixed-max eligibility test, in scaled-logit units (the library's
+# constant; the pages give no value).
+TAU = 40.0
+
+
+def build(force: bool = False) -> str:
+    """Compiles oracle.c into _build/liboracle.so with gcc -O2 -fopenmp."""
+    os.makedirs(_BUILD, exist_ok=True)
+    if (not force and os.path.exists(_LIB_PATH)
+            and os.path.getmtime(_LIB_PATH) >= os.path.getmtime(_SRC)):
+        return _LIB_PATH
+    tmp = _LIB_PATH + f".tmp{os.getpid()}"
+    cmd = ["gcc", "-O2", "-std=c11", "-fopenmp", "-fPIC", "-shared", _SRC, "-o", tmp, "-lm"]
+    subprocess.run(cmd, check=True)
+    os.replace(tmp, _LIB_PATH)
+    return _LIB_PATH
+
+
+def _load():
+    global _lib
+    with _lock:
+        if _lib is None:
+            lib = ctypes.CDLL(build())
+            L, P, D = ctypes.c_long, ctypes.c_void_p, ctypes.c_double
+            lib.orc_mask.argtypes = [L, L, L, L, L, L]
+            lib.orc_mask.restype = ctypes.c_int
+            lib.orc_mask_dense.argtypes = [L, L, L, L, P]
+            lib.orc_blockmap.argtypes = [L, L, L, L, L, L, P, P, P, L, P]
+            lib.orc_blockmap.restype = ctypes.c_int
+            lib.orc_prepare.argtypes = [P, P, L, L, L, D, D, P, P, P, P, P, P]
+            lib.orc_attention_rows.argtypes = [P, P, P, L, L, L, L, L, L, D, L, P, P, P]
+            lib.orc_attention_rows_fixed.argtypes = [P, P, P, P, P, L, L, L, L, L, L, D, L,
+                                                     P, P, P]
+            lib.orc_attention_rows_online.argtypes = [P, P, P, L, L, L, L, L, L, D, L, L, P,
+                                                      P, P]
+            lib.orc_num_threads.restype = ctypes.c_int
+            _lib = lib
+    return _lib
+
+
+def num_threads() -> int:
+    return int(_load().orc_num_threads())
+
+
+def _ptr(a: np.ndarray):
+    return ctypes.c_void_p(a.ctypes.data)
+
+
+def as_f64(x) -> np.ndarray:
+    """[..., N, D] bf16/float tensor or array -> contiguous float64 [nbh, N, D]
+    (exact for bf16 and fp32 inputs)."""
+    if isinstance(x, torch.Tensor):
+        x = x.detach().to("cpu").to(torch.float64).numpy()
+    x = np.ascontiguousarray(x, dtype=np.float64)
+    return x.reshape(-1, x.shape[-2], x.shape[-1])
+
+
+def mask(F, T, w, R, i, j) -> int:
+    return int(_load().orc_mask(F, T, w, R, i, j))
+
+
+def mask_dense(F, T, w, R) -> np.ndarray:
+    n = (F + R) * T
+    out = np.zeros((n, n), dtype=np.uint8)
+    _load().orc_mask_dense(F, T, w, R, _ptr(out))
+    return out
+
+
+def blockmap(F, T, w, R, bq, bk) -> dict:
+    n = (F + R) * T
+    if bq <= 0 or bk <= 0 or n % bq or n % bk:
+        raise ValueError("block sizes must tile the sequence")
+    nqb, nkb = n // bq, n // bk
+    bitmap = np.zeros(nqb * nkb, dtype=np.uint8)
+    row_ptr = np.zeros(nqb + 1, dtype=np.int32)
+    col = np.zeros(nqb * nkb, dtype=np.int32)
+    counts = np.zeros(4, dtype=np.int64)
+    rc = _load().orc_blockmap(F, T, w, R, bq, bk, _ptr(bitmap), _ptr(row_ptr), _ptr(col),
+                              nqb * nkb, _ptr(counts))
+    if rc != 0:
+        raise RuntimeError("orc_blockmap failed")
+    nnz = int(counts[3])
+    return {"bitmap": bitmap.reshape(nqb, nkb), "row_ptr": row_ptr, "col": col[:nnz].copy(),
+            "full": int(counts[0]), "empty": int(counts[1]), "partial": int(counts[2]),
+            "nnz": nnz}
+
+
+def prepare(q, k, scale: float, tau: float = TAU) -> dict:
+    """fp64 per-head statistics; q, k are [..., N, D]."""
+    qd, kd = as_f64(q), as_f64(k)
+    nbh, n, d = kd.shape
+    mu = np.zeros((nbh, d)); kmax = np.zeros(nbh); qn = np.zeros((nbh, n))
+    b = np.zeros((nbh, n)); bmax = np.zeros(nbh); elig = np.zeros(nbh, dtype=np.uint8)
+    _load().orc_prepare(_ptr(qd), _ptr(kd), nbh, n, d, scale, tau, _ptr(mu), _ptr(kmax),
+                        _ptr(qn), _ptr(b), _ptr(bmax), _ptr(elig))
+    return {"mu": mu, "kmax": kmax, "qn": qn, "b": b, "bmax": bmax, "elig": elig}
+
+
+def _pairs(pairs):
+    p = np.asarray(pairs, dtype=np.int64).reshape(-1, 2)
+    return np.ascontiguousarray(p[:, 0]), np.ascontiguousarray(p[:, 1])
+
+
+def attention_rows(q, k, v, F, T, w, R, scale, pairs) -> np.ndarray:
+    """Plain masked softmax attention for (head, row) pairs -> [npairs, D].
+    Heads index the flattened [nbh] axis of q, k, v."""
+    qd, kd, vd = as_f64(q), as_f64(k), as_f64(v)
+    nbh, n, d = kd.shape
+    h, r = _pairs(pairs)
+    out = np.zeros((len(h), d))
+    _load().orc_attention_rows(_ptr(qd), _ptr(kd), _ptr(vd), n, d, F, T, w, R, scale, len(h),
+                               _ptr(h), _ptr(r), _ptr(out))
+    return out
+
+
+def attention_rows_fixed(q, k, v, F, T, w, R, scale, pairs, stats) -> np.ndarray:
+    qd, kd, vd = as_f64(q), as_f64(k), as_f64(v)
+    nbh, n, d = kd.shape
+    h, r = _pairs(pairs)
+    mu = np.ascontiguousarray(stats["mu"], dtype=np.float64)
+    b = np.ascontiguousarray(stats["b"], dtype=np.float64)
+    out = np.zeros((len(h), d))
+    _load().orc_attention_rows_fixed(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(mu), _ptr(b), n, d, F,
+                                     T, w, R, scale, len(h), _ptr(h), _ptr(r), _ptr(out))
+    return out
+
+
+def attention_rows_online(q, k, v, F, T, w, R, scale, bk, pairs) -> np.ndarray:
+    qd, kd, vd = as_f64(q), as_f64(k), as_f64(v)
+    nbh, n, d = kd.shape
+    h, r = _pairs(pairs)
+    out = np.zeros((len(h), d))
+    _load().orc_attention_rows_online(_ptr(qd), _ptr(kd), _ptr(vd), n, d, F, T, w, R, scale,
+                                      bk, len(h), _ptr(h), _ptr(r), _ptr(out))
+    return out
+
+
+def attention_full(q, k, v, F, T, w, R, scale) -> np.ndarray:
+    """Every row of every head: [nbh, N, D] (small shapes)."""
+    kd = as_f64(k)
+    nbh, n, d = kd.shape
+    pairs = [(h, i) for h in range(nbh) for i in range(n)]
+    return attention_rows(q, k, v, F, T, w, R, scale, pairs).reshape(nbh, n, d)

@@ -1,0 +1,55 @@
+"""Pure-Python brute force for tiny inputs.
+
+TEST INFRASTRUCTURE ONLY (same rule as the rest of oracle/).  A second,
+independent restatement of the definitions in the Google Developers Blog
+post "HeyGen x Google Cloud: Bringing Avatar IV to TPUs" (section "Deleting
+the mask" for the mask, section "Breaking softmax's dependency chain" for the
+bound), written with Python lists, loops and math.exp only, so that the C
+oracle can be checked against it on tiny shapes.
+"""
+from __future__ import annotations
+
+import math
+
+
+def frame_of(tok: int, T: int) -> int:
+    return tok // T
+
+
+def attends(i: int, j: int, T: int, w: int, R: int) -> bool:
+    """Query token i sees key token j: key in a reference frame, or query in a
+    reference frame, or the two video frames at most w apart."""
+    fi, fj = frame_of(i, T), frame_of(j, T)
+    if fj < R or fi < R:
+        return True
+    return abs((fi - R) - (fj - R)) <= w
+
+
+def mask(F: int, T: int, w: int, R: int):
+    n = (F + R) * T
+    return [[1 if attends(i, j, T, w, R) else 0 for j in range(n)] for i in range(n)]
+
+
+def attention(q, k, v, F, T, w, R, scale):
+    """q, k, v: nested lists [N][D] for one head.  Returns [N][D]."""
+    n, d = len(q), len(q[0])
+    out = []
+    for i in range(n):
+        logits = []
+        for j in range(n):
+            if attends(i, j, T, w, R):
+                logits.append((j, scale * sum(q[i][c] * k[j][c] for c in range(d))))
+        top = max(s for _, s in logits)
+        weights = [(j, math.exp(s - top)) for j, s in logits]
+        den = sum(e for _, e in weights)
+        out.append([sum(e * v[j][c] for j, e in weights) / den for c in range(d)])
+    return out
+
+
+def key_mean(k):
+    n, d = len(k), len(k[0])
+    return [sum(k[j][c] for j in range(n)) / n for c in range(d)]
+
+
+def norm(x):
+    return math.sqrt(sum(t * t for t in x))
