@@ -1,0 +1,410 @@
+"""Benchmark of the frame-aligned window-sparse attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--impl wsattn|reference]
+                    [--workload sr] [--block-k 0] [--no-cpu-baseline]
+
+A step is one pass of the whole hot path over one batch of synthetic input:
+wsattn_prepare (key mean, row bounds, eligibility) + wsattn_forward (fused
+tcgen05 attention) through the C ABI, on inputs already resident in HBM.  The
+plan (block map) is built once per shape, outside the timed region.
+
+Metric: effective TFLOP/s on active blocks = 4 * D * (active query-key pairs)
+* B * H per step / step time.  Inputs (q, k, v 140 MB each, out 281 MB at the
+SR shape) are larger than L2, so no flush runs between steps.
+
+Under torchrun every rank runs its own replica of the workload (the path has
+no exchange step); value = work of all ranks / the slowest rank's time.
+`--impl reference` times the CPU oracle (the reference arm of this build) on
+a bounded row sample of the same workload instead.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "effective TFLOP/s on active blocks & % of GB300 bf16 peak; ms/call at SR shape"
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
+
+# dram__bytes_read.sum + dram__bytes_write.sum of one forward launch, from an
+# ncu capture, keyed by workload; valid only for the kernel source it was
+# measured on (sha256 of forward.cu, first 16 hex digits).
+FORWARD_TRAFFIC = {}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "bf16_tflops": float(d["bf16_tflops"]),
+                "source": "measured"}
+    except (OSError, KeyError, ValueError):
+        return dict(FALLBACK_PEAKS, source="fallback")
+
+
+def _forward_src_hash():
+    with open(os.path.join(ROOT, "frame_aligned_window_gb300", "csrc", "forward.cu"), "rb") as f:
+        return hashlib.sha256(f.read()).hexdigest()[:16]
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons, sampled every 200 ms."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu = gpu_index
+        self.proc = None
+        self.lines = []
+        self.t_start = self.t_stop = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.gpu)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self.reader = threading.Thread(target=self._read, daemon=True)
+        self.reader.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append((time.time(), line.strip()))
+
+    def mark_start(self):
+        self.t_start = time.time()
+
+    def mark_stop(self):
+        self.t_stop = time.time()
+
+    def stop(self):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        rows = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            rows.append((t, parts))
+        inside = [r for t, r in rows if self.t_start and self.t_stop
+                  and self.t_start - 0.2 <= t <= self.t_stop + 0.2]
+        use = inside or [r for _, r in rows]
+        if not use:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["no samples"]}
+
+        def num(x):
+            try:
+                return float(x)
+            except ValueError:
+                return None
+        sm = [num(r[1]) for r in use if num(r[1]) is not None]
+        mx = [num(r[2]) for r in use if num(r[2]) is not None]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for r in use for i in range(4) if r[5 + i] == "Active"})
+        pw = [num(r[3]) for r in use if num(r[3]) is not None]
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(mx) if mx else None,
+                "power_w_max": max(pw) if pw else None,
+                "reasons": reasons, "samples": len(use),
+                "samples_in_timed_region": len(inside)}
+
+
+def _dist():
+    import torch
+    import torch.distributed as dist
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and not dist.is_initialized():
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        dist.init_process_group(backend)
+    return world, rank, local
+
+
+def max_over_ranks(x: float, world: int) -> float:
+    """Largest value of x across ranks (the job's time is its slowest rank's)."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def step_flops(wl, active_pairs: int) -> float:
+    return 4.0 * wl.head_dim * active_pairs * wl.batch * wl.heads
+
+
+# --------------------------------------------------------------- CPU oracle
+def oracle_timing(wl, budget_s: float, min_rows: int = 16):
+    """Times the oracle on whole heads' rows until `budget_s` is spent.
+    Returns (TFLOP/s, seconds, sample description, threads)."""
+    import numpy as np
+    import oracle
+    from workloads import generate
+
+    q, k, v = generate(wl)
+    F, T, w, R = wl.frames, wl.tokens_per_frame, wl.window, wl.ref_frames
+    n = wl.n_tokens
+    m_frames = oracle.blockmap(F, 1, w, R, 1, 1)
+    row_pairs = np.zeros(n, dtype=np.int64)  # active keys per query row
+    bm = m_frames["bitmap"]
+    for a in range(F + R):
+        row_pairs[a * T:(a + 1) * T] = int(bm[a].sum()) * T
+    qf = q.reshape(-1, n, wl.head_dim)
+    kf = k.reshape(-1, n, wl.head_dim)
+    vf = v.reshape(-1, n, wl.head_dim)
+    flops = 0.0
+    rows_done = 0
+    heads_done = 0
+    t_total = 0.0
+    chunk = 2048
+    h = 0
+    while True:
+        qs, ks, vs = qf[h:h + 1], kf[h:h + 1], vf[h:h + 1]
+        for r0 in range(0, n, chunk):
+            rows = list(range(r0, min(n, r0 + chunk)))
+            t0 = time.perf_counter()
+            oracle.attention_rows(qs, ks, vs, F, T, w, R, wl.scale, [(0, r) for r in rows])
+            t_total += time.perf_counter() - t0
+            flops += 4.0 * wl.head_dim * float(row_pairs[rows].sum())
+            rows_done += len(rows)
+            if t_total >= budget_s and rows_done >= min_rows:
+                break
+        if rows_done == (h + 1) * n:
+            heads_done += 1
+        h += 1
+        if t_total >= budget_s or h >= qf.shape[0]:
+            break
+    sample = (f"{rows_done} query rows ({heads_done} whole heads) of {wl.label()}, "
+              f"rows in token order, each against every active key")
+    return flops / t_total / 1e12, t_total, sample, oracle.num_threads()
+
+
+def run_reference(args, wl, world, rank):
+    """The reference arm: the CPU oracle, on rank 0 only."""
+    if rank != 0:
+        return
+    import oracle
+    oracle.build()
+    per_step = max(0.05, min(2.0, 120.0 / max(1, args.steps + args.warmup)))
+    for _ in range(args.warmup):
+        oracle_timing(wl, per_step * 0.2, min_rows=16)
+    vals = []
+    secs = 0.0
+    sample = ""
+    threads = 1
+    for _ in range(args.steps):
+        v, s, sample, threads = oracle_timing(wl, per_step, min_rows=16)
+        vals.append(v)
+        secs += s
+    value = statistics.median(vals)
+    line = {
+        "impl": "reference", "metric": METRIC, "value": value, "unit": "TFLOP/s",
+        "n_gpus": 1, "steps": args.steps, "warmup": args.warmup,
+        "ms_per_step": secs / max(1, args.steps) * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+        "config": {"workload": wl.label(), "block_k": None,
+                   "l2": "CPU run; no GPU caches involved"},
+        "cpu_baseline": {"value": value, "unit": "TFLOP/s", "cores": threads, "kind": "oracle",
+                         "sample": f"per step: {sample}"},
+        "e2e": {"value": value, "unit": "TFLOP/s", "h2d_bytes_per_step": 0,
+                "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+# ------------------------------------------------------------------ GPU arm
+def run_gpu(args, wl, world, rank, local):
+    import torch
+
+    import frame_aligned_window_gb300 as fw
+    from workloads import generate
+
+    torch.cuda.set_device(local)
+    dev = torch.device("cuda", local)
+    q, k, v = generate(wl)
+    q_h, k_h, v_h = (x.pin_memory() for x in (q, k, v))
+    qd, kd, vd = (x.to(dev) for x in (q, k, v))
+    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    out_h = torch.empty(q.shape, dtype=torch.float32).pin_memory()
+    plan = fw.wsattn_plan(wl.frames, wl.tokens_per_frame, wl.window, wl.ref_frames, wl.heads,
+                          wl.head_dim, 0, args.block_k)
+    flops = step_flops(wl, plan.active_pairs)
+    stream = torch.cuda.current_stream()
+
+    def step():
+        fw.wsattn_prepare(plan, qd, kd)
+        fw.wsattn_forward(plan, qd, kd, vd, out)
+
+    for _ in range(max(3, args.warmup)):
+        step()
+    torch.cuda.synchronize()
+    assert fw.wsattn_device_status(plan) == 0
+
+    clocks = ClockSampler(local) if rank == 0 else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.6)  # let the sampler start before the timed region
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    _barrier(world)
+    torch.cuda.synchronize()
+    if clocks:
+        clocks.mark_start()
+    t_begin = torch.cuda.Event(enable_timing=True)
+    t_end = torch.cuda.Event(enable_timing=True)
+    t_begin.record(stream)
+    for i in range(args.steps):
+        e0, e1, e2 = ev[i]
+        e0.record(stream)
+        fw.wsattn_prepare(plan, qd, kd)
+        e1.record(stream)
+        fw.wsattn_forward(plan, qd, kd, vd, out)
+        e2.record(stream)
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    if clocks:
+        clocks.mark_stop()
+    status = fw.wsattn_device_status(plan)
+    if status != 0:
+        raise RuntimeError(f"device status: {fw.wsattn_status_string(status)}")
+    total_ms = t_begin.elapsed_time(t_end)
+    prep_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev]
+    fwd_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev]
+    ms_step = max_over_ranks(total_ms / args.steps, world)
+
+    # end to end through the public API: pinned host inputs in, result out
+    e2e_steps = max(3, min(args.steps, 20))
+    e_begin = torch.cuda.Event(enable_timing=True)
+    e_end = torch.cuda.Event(enable_timing=True)
+    _barrier(world)
+    torch.cuda.synchronize()
+    e_begin.record(stream)
+    for _ in range(e2e_steps):
+        qd.copy_(q_h, non_blocking=True)
+        kd.copy_(k_h, non_blocking=True)
+        vd.copy_(v_h, non_blocking=True)
+        fw.wsattn_prepare(plan, qd, kd)
+        fw.wsattn_forward(plan, qd, kd, vd, out)
+        out_h.copy_(out, non_blocking=True)
+    e_end.record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    e2e_ms = max_over_ranks(e_begin.elapsed_time(e_end) / e2e_steps, world)
+    if clocks:
+        clocks.stop()
+
+    if rank != 0:
+        return None
+    peaks = _peaks()
+    fwd_avg = statistics.mean(fwd_ms)
+    prep_avg = statistics.mean(prep_ms)
+    achieved = flops / (fwd_avg * 1e-3) / 1e12
+    elem = q.numel()
+    prep_bytes = 3 * elem * 2 + 2 * wl.batch * wl.heads * wl.n_tokens * 4
+    src = _forward_src_hash()
+    traffic = FORWARD_TRAFFIC.get((wl.name, plan.block_k, src))
+    line = {
+        "metric": METRIC,
+        "value": flops * world / (ms_step * 1e-3) / 1e12,
+        "unit": "TFLOP/s",
+        "n_gpus": world,
+        "steps": args.steps,
+        "warmup": args.warmup,
+        "ms_per_step": ms_step,
+        "higher_is_better": True,
+        "scaling": "weak",
+        "vs_baseline": None,
+        "dtype": "bf16",
+        "data": "synthetic",
+        "config": {"workload": wl.label(), "block_q": plan.block_q, "block_k": plan.block_k,
+                   "gflop_per_step": flops / 1e9,
+                   "l2": "inputs larger than L2 (q, k, v, out = %.0f MB); no flush"
+                         % ((3 * elem * 2 + elem * 4) / 1e6),
+                   "per_rank": "independent replica"},
+        "roofline": {"bound": "tensor", "kernel": "wsattn_fwd_kernel", "achieved": achieved,
+                     "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
+                     "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                     "peak_source": f"{peaks['source']} (bf16 burst)",
+                     "ms_per_launch": fwd_avg},
+        "prepare": {"bound": "hbm", "ms_per_call": prep_avg, "launches": 3,
+                    "algorithmic_bytes": prep_bytes,
+                    "achieved": prep_bytes / (prep_avg * 1e-3) / 1e9,
+                    "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                    "frac": prep_bytes / (prep_avg * 1e-3) / 1e9 / peaks["hbm_gbs"]},
+        "e2e": {"value": flops * world / (e2e_ms * 1e-3) / 1e12, "unit": "TFLOP/s",
+                "ms_per_step": e2e_ms, "h2d_bytes_per_step": 3 * elem * 2,
+                "d2h_bytes_per_step": elem * 4},
+        "gpu_launches": 4 * args.steps,
+        "clocks": clocks.summary() if clocks else None,
+    }
+    return line
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=300)
+    ap.add_argument("--warmup", type=int, default=10)
+    ap.add_argument("--impl", default="wsattn", choices=["wsattn", "reference"])
+    ap.add_argument("--workload", default="sr")
+    ap.add_argument("--block-k", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--cpu-budget", type=float, default=12.0,
+                    help="seconds of oracle time for the cpu_baseline sample")
+    args = ap.parse_args()
+    from workloads import WORKLOADS
+    wl = WORKLOADS[args.workload]
+    world, rank, local = _dist()
+    if args.impl == "reference":
+        run_reference(args, wl, world, rank)
+        return
+    line = run_gpu(args, wl, world, rank, local)
+    if rank == 0 and line is not None:
+        if not args.no_cpu_baseline and world == 1:
+            v, secs, sample, threads = oracle_timing(wl, args.cpu_budget)
+            line["cpu_baseline"] = {"value": v, "unit": "TFLOP/s", "cores": threads,
+                                    "kind": "oracle", "sample": sample,
+                                    "seconds": secs}
+        print(json.dumps(line), flush=True)
+    if world > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+if __name__ == "__main__":
+    main()

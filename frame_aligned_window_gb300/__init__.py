@@ -1,0 +1,229 @@
+"""Python binding of libwsattn (frame-aligned window-sparse attention, GB300).
+
+Argument marshalling only: every step of the computation runs in the CUDA
+library (include/wsattn.h documents each call).  Tensors are torch tensors
+used as device memory; the current torch CUDA stream is passed to the
+library.  If libwsattn.so is missing or fails to load, importing this
+package raises: there is no fallback implementation.
+
+The names mirror the C ABI:
+    wsattn_plan, wsattn_plan_destroy, wsattn_prepare, wsattn_forward,
+    wsattn_plan_info, wsattn_get_block_map, wsattn_get_csr, wsattn_get_stats,
+    wsattn_plan_set_debug, wsattn_device_status, wsattn_selftest_timeout,
+    wsattn_status_string
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import numpy as np
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libwsattn.so")
+
+# C ABI entry points declared in include/wsattn.h
+EXPORTS = (
+    "wsattn_plan", "wsattn_plan_destroy", "wsattn_prepare", "wsattn_forward",
+    "wsattn_plan_info", "wsattn_get_block_map", "wsattn_get_csr", "wsattn_get_stats",
+    "wsattn_plan_set_debug", "wsattn_device_status", "wsattn_selftest_timeout",
+    "wsattn_status_string",
+)
+
+STATUS = {0: "OK", 1: "BAD_ARG", 2: "BAD_BLOCK", 3: "UNSUPPORTED", 4: "NOT_PREPARED",
+          5: "BATCH_MISMATCH", 6: "CUDA", 7: "TIMEOUT", 8: "NO_MEMORY"}
+
+
+class WsattnError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        self.code = code
+        super().__init__(f"{what}: {STATUS.get(code, code)} ({status_text(code)})")
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"{LIB_PATH} is missing: build it with "
+                      "`python frame_aligned_window_gb300/build.py`")
+_lib = ctypes.CDLL(LIB_PATH)
+
+_P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
+_lib.wsattn_plan.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_P)]
+_lib.wsattn_plan_destroy.argtypes = [_P]
+_lib.wsattn_prepare.argtypes = [_P, _I, _P, _P, _P]
+_lib.wsattn_forward.argtypes = [_P, _I, _P, _P, _P, _P, _P]
+_lib.wsattn_plan_info.argtypes = [_P, _P, _I]
+_lib.wsattn_get_block_map.argtypes = [_P, _P, _SZ]
+_lib.wsattn_get_csr.argtypes = [_P, _P, _P, _SZ, _SZ]
+_lib.wsattn_get_stats.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P]
+_lib.wsattn_plan_set_debug.argtypes = [_P, _I, _F]
+_lib.wsattn_device_status.argtypes = [_P, _P]
+_lib.wsattn_selftest_timeout.argtypes = [_I, ctypes.POINTER(_I), _P]
+_lib.wsattn_status_string.argtypes = [_I]
+_lib.wsattn_status_string.restype = ctypes.c_char_p
+for _name in EXPORTS:
+    if _name != "wsattn_status_string":
+        getattr(_lib, _name).restype = _I
+
+
+def status_text(code: int) -> str:
+    return _lib.wsattn_status_string(int(code)).decode()
+
+
+def wsattn_status_string(code: int) -> str:
+    return status_text(code)
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        raise WsattnError(rc, what)
+
+
+class Plan:
+    """Owns a wsattn_plan_t handle (released by destroy() or on collection)."""
+
+    def __init__(self, handle, args):
+        self._h = handle
+        self.args = args
+        info = np.zeros(10, dtype=np.int64)
+        _check(_lib.wsattn_plan_info(self._h, info.ctypes.data, 10), "wsattn_plan_info")
+        (self.n_tokens, self.block_q, self.block_k, self.n_qblocks, self.n_kblocks, self.nnz,
+         self.tiles_per_head, self.head_dim, self.heads, self.active_pairs) = (int(x) for x in info)
+        self.frames, self.tokens_per_frame, self.window, self.ref_frames = args[:4]
+
+    @property
+    def handle(self):
+        if self._h is None:
+            raise ValueError("plan was destroyed")
+        return self._h
+
+    def destroy(self):
+        if self._h is not None:
+            _lib.wsattn_plan_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.destroy()
+        except Exception:
+            pass
+
+
+def _stream_ptr(stream):
+    import torch
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _dev_ptr(t, name, dtype=None):
+    import torch
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise TypeError(f"{name} must be a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name} must be contiguous")
+    if dtype is not None and t.dtype != dtype:
+        raise TypeError(f"{name} must be {dtype}, got {t.dtype}")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _check_shape(plan: Plan, t, name):
+    if t.dim() != 4 or t.shape[1] != plan.heads or t.shape[2] != plan.n_tokens \
+            or t.shape[3] != plan.head_dim:
+        raise ValueError(f"{name} must be [B, {plan.heads}, {plan.n_tokens}, {plan.head_dim}], "
+                         f"got {tuple(t.shape)}")
+
+
+def wsattn_plan(frames, tokens_per_frame, window, ref_frames, heads, head_dim, block_q=0,
+                block_k=0) -> Plan:
+    h = _P()
+    args = (frames, tokens_per_frame, window, ref_frames, heads, head_dim, block_q, block_k)
+    _check(_lib.wsattn_plan(*args, ctypes.byref(h)), "wsattn_plan")
+    return Plan(h, args)
+
+
+def wsattn_plan_destroy(plan: Plan):
+    plan.destroy()
+
+
+def wsattn_prepare(plan: Plan, q, k, stream=None):
+    """Key mean, row bounds, row fixed max and per-head eligibility (q, k read only)."""
+    import torch
+    _check_shape(plan, q, "q")
+    _check_shape(plan, k, "k")
+    if q.shape[0] != k.shape[0]:
+        raise ValueError("q and k batch differ")
+    _check(_lib.wsattn_prepare(plan.handle, q.shape[0], _dev_ptr(q, "q", torch.bfloat16),
+                               _dev_ptr(k, "k", torch.bfloat16), _stream_ptr(stream)),
+           "wsattn_prepare")
+
+
+def wsattn_forward(plan: Plan, q, k, v, out=None, stream=None):
+    import torch
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_shape(plan, t, n)
+    if not (q.shape[0] == k.shape[0] == v.shape[0]):
+        raise ValueError("q, k, v batch differ")
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=q.device)
+    _check_shape(plan, out, "out")
+    _check(_lib.wsattn_forward(plan.handle, q.shape[0], _dev_ptr(q, "q", torch.bfloat16),
+                               _dev_ptr(k, "k", torch.bfloat16), _dev_ptr(v, "v", torch.bfloat16),
+                               _dev_ptr(out, "out", torch.float32), _stream_ptr(stream)),
+           "wsattn_forward")
+    return out
+
+
+def wsattn_plan_info(plan: Plan) -> dict:
+    return {"n_tokens": plan.n_tokens, "block_q": plan.block_q, "block_k": plan.block_k,
+            "n_qblocks": plan.n_qblocks, "n_kblocks": plan.n_kblocks, "nnz": plan.nnz,
+            "tiles_per_head": plan.tiles_per_head, "head_dim": plan.head_dim,
+            "heads": plan.heads, "active_pairs": plan.active_pairs}
+
+
+def wsattn_get_block_map(plan: Plan) -> np.ndarray:
+    out = np.zeros((plan.n_qblocks, plan.n_kblocks), dtype=np.uint8)
+    _check(_lib.wsattn_get_block_map(plan.handle, out.ctypes.data, out.size),
+           "wsattn_get_block_map")
+    return out
+
+
+def wsattn_get_csr(plan: Plan):
+    row_ptr = np.zeros(plan.n_qblocks + 1, dtype=np.int32)
+    col = np.zeros(max(plan.nnz, 1), dtype=np.int32)
+    _check(_lib.wsattn_get_csr(plan.handle, row_ptr.ctypes.data, col.ctypes.data, row_ptr.size,
+                               col.size), "wsattn_get_csr")
+    return row_ptr, col[:plan.nnz]
+
+
+def wsattn_get_stats(plan: Plan, batch: int, stream=None) -> dict:
+    bh = batch * plan.heads
+    b = np.zeros((bh, plan.n_tokens), dtype=np.float32)
+    m = np.zeros((bh, plan.n_tokens), dtype=np.float32)
+    mu = np.zeros((bh, plan.head_dim), dtype=np.float32)
+    kmax = np.zeros(bh, dtype=np.float32)
+    bmax = np.zeros(bh, dtype=np.float32)
+    elig = np.zeros(bh, dtype=np.uint8)
+    _check(_lib.wsattn_get_stats(plan.handle, b.ctypes.data, m.ctypes.data, mu.ctypes.data,
+                                 kmax.ctypes.data, bmax.ctypes.data, elig.ctypes.data,
+                                 _stream_ptr(stream)), "wsattn_get_stats")
+    return {"b": b, "m": m, "mu": mu, "kmax": kmax, "bmax": bmax, "elig": elig}
+
+
+def wsattn_plan_set_debug(plan: Plan, force_path: int = -1, tau: float = 0.0):
+    _check(_lib.wsattn_plan_set_debug(plan.handle, int(force_path), float(tau)),
+           "wsattn_plan_set_debug")
+
+
+def wsattn_device_status(plan: Plan, stream=None) -> int:
+    return int(_lib.wsattn_device_status(plan.handle, _stream_ptr(stream)))
+
+
+def wsattn_selftest_timeout(limit_ms: int = 50, stream=None) -> int:
+    st = _I(-1)
+    _check(_lib.wsattn_selftest_timeout(int(limit_ms), ctypes.byref(st), _stream_ptr(stream)),
+           "wsattn_selftest_timeout")
+    return int(st.value)
+
+
+def raw_call(name: str):
+    """The ctypes function for an exported symbol (for tests of the ABI)."""
+    return getattr(_lib, name)

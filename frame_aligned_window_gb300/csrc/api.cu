@@ -1,0 +1,366 @@
+// C ABI of libwsattn (declared in include/wsattn.h): plan lifecycle, device
+// buffers, TMA tensor maps and kernel launches.  Nothing here computes on the
+// host beyond argument checks and the block map (plan.cpp).
+#include <cudaTypedefs.h>
+
+#include <cmath>
+#include <cstring>
+#include <mutex>
+#include <new>
+
+#include "internal.h"
+
+using wsattn::FwdParams;
+using wsattn::HostPlan;
+using wsattn::PrepBuffers;
+using wsattn::WorkTile;
+
+struct wsattn_plan_s {
+  HostPlan hp;
+  int device = -1;
+  int num_sms = 0;
+  size_t smem_optin = 0;
+  int clock_khz = 0;
+  WorkTile* d_tiles = nullptr;
+  int32_t* d_kcol = nullptr;
+  int* d_status = nullptr;
+  // statistics workspace, sized for ws_batch
+  int ws_batch = 0;
+  void* ws = nullptr;
+  PrepBuffers buf{};
+  int prepared_batch = 0;
+  int force_path = -1;
+  float tau = wsattn::kDefaultTau;
+};
+
+namespace {
+
+PFN_cuTensorMapEncodeTiled_v12000 g_encode = nullptr;
+std::once_flag g_encode_once;
+
+bool get_encode() {
+  std::call_once(g_encode_once, [] {
+    void* fn = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &fn, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      g_encode = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(fn);
+  });
+  return g_encode != nullptr;
+}
+
+bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
+
+// 2-D view [rows, D] of a bf16 tensor; box {64, box_rows}; 128-byte swizzle.
+bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int D, int box_rows) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
+  const cuuint32_t box[2] = {64, static_cast<cuuint32_t>(box_rows)};
+  const cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// First device call: remember the device, upload the work list.
+int ensure_device(wsattn_plan_s* p) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return WSATTN_ERR_CUDA;
+  if (p->device >= 0) return dev == p->device ? WSATTN_OK : WSATTN_ERR_BAD_ARG;
+  int sms = 0, optin = 0, clk = 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&optin, cudaDevAttrMaxSharedMemoryPerBlockOptin, dev) !=
+          cudaSuccess ||
+      cudaDeviceGetAttribute(&clk, cudaDevAttrClockRate, dev) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  const HostPlan& hp = p->hp;
+  const size_t tiles_bytes = hp.tiles.size() * sizeof(WorkTile);
+  const size_t kcol_bytes = hp.kcol.size() * sizeof(int32_t);
+  if (cudaMalloc(&p->d_tiles, tiles_bytes) != cudaSuccess ||
+      cudaMalloc(&p->d_kcol, kcol_bytes) != cudaSuccess ||
+      cudaMalloc(&p->d_status, sizeof(int)) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  if (cudaMemcpy(p->d_tiles, hp.tiles.data(), tiles_bytes, cudaMemcpyHostToDevice) !=
+          cudaSuccess ||
+      cudaMemcpy(p->d_kcol, hp.kcol.data(), kcol_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  p->device = dev;
+  p->num_sms = sms;
+  p->smem_optin = static_cast<size_t>(optin);
+  p->clock_khz = clk;
+  return WSATTN_OK;
+}
+
+// Statistics workspace for `batch`; growing it synchronises the stream.
+int ensure_workspace(wsattn_plan_s* p, int batch, cudaStream_t stream) {
+  if (batch <= p->ws_batch) return WSATTN_OK;
+  const HostPlan& hp = p->hp;
+  const int BH = batch * hp.H;
+  int nchunk = 0, rpc = 0;
+  wsattn::prepare_chunking(BH, hp.N, p->num_sms, &nchunk, &rpc);
+  // Chunk slots: any batch <= this one needs at most BH * ceil(4 SMs / BH)
+  // <= 4 SMs + BH of them (prepare_chunking aims at four waves).
+  size_t slots = static_cast<size_t>(BH) * nchunk;
+  const size_t bound = static_cast<size_t>(4) * p->num_sms + BH;
+  if (slots < bound) slots = bound;
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t n_b = up(sizeof(float) * BH * hp.N);  // b_rows, and again for m_rows
+  const size_t n_mu = up(sizeof(float) * BH * hp.D);
+  const size_t n_h = up(sizeof(float) * BH);
+  const size_t n_el = up(BH);
+  const size_t n_ps = up(sizeof(float) * slots * hp.D);
+  const size_t n_pm = up(sizeof(float) * slots);
+  const size_t total = 2 * n_b + n_mu + 2 * n_h + n_el + n_ps + 2 * n_pm;
+  if (p->ws) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return WSATTN_ERR_CUDA;
+    cudaFree(p->ws);
+    p->ws = nullptr;
+    p->ws_batch = 0;
+  }
+  if (cudaMalloc(&p->ws, total) != cudaSuccess) {
+    p->ws = nullptr;
+    return WSATTN_ERR_CUDA;
+  }
+  char* c = static_cast<char*>(p->ws);
+  PrepBuffers& b = p->buf;
+  b.b_rows = reinterpret_cast<float*>(c); c += n_b;
+  b.m_rows = reinterpret_cast<float*>(c); c += n_b;
+  b.mu = reinterpret_cast<float*>(c); c += n_mu;
+  b.kmax = reinterpret_cast<float*>(c); c += n_h;
+  b.bmax = reinterpret_cast<float*>(c); c += n_h;
+  b.elig = reinterpret_cast<uint8_t*>(c); c += n_el;
+  b.part_sum = reinterpret_cast<float*>(c); c += n_ps;
+  b.part_kmax = reinterpret_cast<float*>(c); c += n_pm;
+  b.part_qmax = reinterpret_cast<float*>(c);
+  b.nchunk = nchunk;
+  b.rows_per_chunk = rpc;
+  p->ws_batch = batch;
+  p->prepared_batch = 0;
+  return WSATTN_OK;
+}
+
+void free_device(wsattn_plan_s* p) {
+  if (p->d_tiles) cudaFree(p->d_tiles);
+  if (p->d_kcol) cudaFree(p->d_kcol);
+  if (p->d_status) cudaFree(p->d_status);
+  if (p->ws) cudaFree(p->ws);
+  p->d_tiles = nullptr;
+  p->d_kcol = nullptr;
+  p->d_status = nullptr;
+  p->ws = nullptr;
+}
+
+}  // namespace
+
+extern "C" {
+
+int wsattn_plan(int frames, int tokens_per_frame, int window, int ref_frames, int heads,
+                int head_dim, int block_q, int block_k, wsattn_plan_t* out) {
+  if (!out) return WSATTN_ERR_BAD_ARG;
+  *out = nullptr;
+  wsattn_plan_s* p = new (std::nothrow) wsattn_plan_s();
+  if (!p) return WSATTN_ERR_NO_MEMORY;
+  const int rc = wsattn::build_host_plan(frames, tokens_per_frame, window, ref_frames, heads,
+                                         head_dim, block_q, block_k, &p->hp);
+  if (rc != WSATTN_OK) {
+    delete p;
+    return rc;
+  }
+  *out = p;
+  return WSATTN_OK;
+}
+
+int wsattn_plan_destroy(wsattn_plan_t plan) {
+  if (!plan) return WSATTN_OK;
+  free_device(plan);
+  delete plan;
+  return WSATTN_OK;
+}
+
+int wsattn_prepare(wsattn_plan_t plan, int batch, const void* q, const void* k, void* stream) {
+  if (!plan || batch < 1 || !q || !k || !aligned16(q) || !aligned16(k)) return WSATTN_ERR_BAD_ARG;
+  const HostPlan& hp = plan->hp;
+  if (static_cast<int64_t>(batch) * hp.H * hp.N >= (int64_t(1) << 31)) return WSATTN_ERR_BAD_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int rc = ensure_device(plan);
+  if (rc != WSATTN_OK) return rc;
+  rc = ensure_workspace(plan, batch, s);
+  if (rc != WSATTN_OK) return rc;
+  const int BH = batch * hp.H;
+  int nchunk = 0, rpc = 0;
+  wsattn::prepare_chunking(BH, hp.N, plan->num_sms, &nchunk, &rpc);
+  PrepBuffers b = plan->buf;
+  b.nchunk = nchunk;
+  b.rows_per_chunk = rpc;
+  const float scale = 1.0f / std::sqrt(static_cast<float>(hp.D));
+  if (wsattn::launch_prepare(q, k, BH, hp.N, hp.D, scale, plan->tau, b, s) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  plan->prepared_batch = batch;
+  return WSATTN_OK;
+}
+
+int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, const void* v,
+                   float* out, void* stream) {
+  if (!plan || batch < 1 || !q || !k || !v || !out) return WSATTN_ERR_BAD_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(out))
+    return WSATTN_ERR_BAD_ARG;
+  const HostPlan& hp = plan->hp;
+  if (plan->prepared_batch == 0) return WSATTN_ERR_NOT_PREPARED;
+  if (batch != plan->prepared_batch) return WSATTN_ERR_BATCH_MISMATCH;
+  if (hp.bk > wsattn::kMaxBlockK) return WSATTN_ERR_UNSUPPORTED;
+  int rc = ensure_device(plan);
+  if (rc != WSATTN_OK) return rc;
+  if (!get_encode()) return WSATTN_ERR_CUDA;
+  const int BH = batch * hp.H;
+  const int64_t rows = static_cast<int64_t>(BH) * hp.N;
+  FwdParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  if (!encode_map(&prm.tm_q, q, rows, hp.D, wsattn::kTileM) ||
+      !encode_map(&prm.tm_k, k, rows, hp.D, hp.bk) || !encode_map(&prm.tm_v, v, rows, hp.D, hp.bk))
+    return WSATTN_ERR_CUDA;
+  prm.tiles = plan->d_tiles;
+  prm.kcol = plan->d_kcol;
+  prm.m_rows = plan->buf.m_rows;
+  prm.elig = plan->buf.elig;
+  prm.out = out;
+  prm.status = plan->d_status;
+  prm.n_tiles = static_cast<int>(hp.tiles.size());
+  prm.bh = BH;
+  prm.n = static_cast<int>(hp.N);
+  prm.bk = hp.bk;
+  wsattn::forward_stages(hp.D, hp.bk, plan->smem_optin, &prm.stages_k, &prm.stages_v);
+  prm.force_path = plan->force_path;
+  prm.scale_log2 = (1.0f / std::sqrt(static_cast<float>(hp.D))) * 1.4426950408889634f;
+  const size_t smem = wsattn::forward_smem_bytes(hp.D, hp.bk, prm.stages_k, prm.stages_v);
+  if (prm.stages_k < 2 || smem > plan->smem_optin) return WSATTN_ERR_UNSUPPORTED;
+  const int64_t items = static_cast<int64_t>(prm.n_tiles) * BH;
+  const int grid = static_cast<int>(items < plan->num_sms ? items : plan->num_sms);
+  if (wsattn::launch_forward(prm, hp.D, grid, smem, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  return WSATTN_OK;
+}
+
+int wsattn_plan_info(wsattn_plan_t plan, int64_t* info, int n) {
+  if (!plan || !info || n < 0) return WSATTN_ERR_BAD_ARG;
+  const HostPlan& hp = plan->hp;
+  const int64_t v[10] = {hp.N,
+                         hp.bq,
+                         hp.bk,
+                         hp.nqb,
+                         hp.nkb,
+                         static_cast<int64_t>(hp.col.size()),
+                         static_cast<int64_t>(hp.tiles.size()),
+                         hp.D,
+                         hp.H,
+                         hp.active_pairs};
+  for (int i = 0; i < n && i < 10; ++i) info[i] = v[i];
+  return WSATTN_OK;
+}
+
+int wsattn_get_block_map(wsattn_plan_t plan, uint8_t* host, size_t n) {
+  if (!plan || !host || n < plan->hp.bitmap.size()) return WSATTN_ERR_BAD_ARG;
+  std::memcpy(host, plan->hp.bitmap.data(), plan->hp.bitmap.size());
+  return WSATTN_OK;
+}
+
+int wsattn_get_csr(wsattn_plan_t plan, int32_t* row_ptr, int32_t* col, size_t n_row_ptr,
+                   size_t n_col) {
+  if (!plan || !row_ptr || (!col && !plan->hp.col.empty())) return WSATTN_ERR_BAD_ARG;
+  if (n_row_ptr < plan->hp.row_ptr.size() || n_col < plan->hp.col.size())
+    return WSATTN_ERR_BAD_ARG;
+  std::memcpy(row_ptr, plan->hp.row_ptr.data(), plan->hp.row_ptr.size() * sizeof(int32_t));
+  if (!plan->hp.col.empty())
+    std::memcpy(col, plan->hp.col.data(), plan->hp.col.size() * sizeof(int32_t));
+  return WSATTN_OK;
+}
+
+int wsattn_get_stats(wsattn_plan_t plan, float* b_rows, float* m_rows, float* mu, float* kmax,
+                     float* bmax, uint8_t* elig, void* stream) {
+  if (!plan) return WSATTN_ERR_BAD_ARG;
+  if (plan->prepared_batch == 0) return WSATTN_ERR_NOT_PREPARED;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  const HostPlan& hp = plan->hp;
+  const size_t BH = static_cast<size_t>(plan->prepared_batch) * hp.H;
+  const PrepBuffers& b = plan->buf;
+  if (b_rows && cudaMemcpy(b_rows, b.b_rows, BH * hp.N * sizeof(float),
+                           cudaMemcpyDeviceToHost) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  if (m_rows && cudaMemcpy(m_rows, b.m_rows, BH * hp.N * sizeof(float),
+                           cudaMemcpyDeviceToHost) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  if (mu && cudaMemcpy(mu, b.mu, BH * hp.D * sizeof(float), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  if (kmax && cudaMemcpy(kmax, b.kmax, BH * sizeof(float), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  if (bmax && cudaMemcpy(bmax, b.bmax, BH * sizeof(float), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  if (elig && cudaMemcpy(elig, b.elig, BH, cudaMemcpyDeviceToHost) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  return WSATTN_OK;
+}
+
+int wsattn_plan_set_debug(wsattn_plan_t plan, int force_path, float tau) {
+  if (!plan || force_path < -1 || force_path > 1 || !(tau >= 0.0f)) return WSATTN_ERR_BAD_ARG;
+  plan->force_path = force_path;
+  if (tau > 0.0f) plan->tau = tau;
+  return WSATTN_OK;
+}
+
+int wsattn_device_status(wsattn_plan_t plan, void* stream) {
+  if (!plan) return WSATTN_ERR_BAD_ARG;
+  if (plan->device < 0) return WSATTN_OK;
+  if (cudaStreamSynchronize(static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  int st = 0;
+  if (cudaMemcpy(&st, plan->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  if (st == 0) return WSATTN_OK;
+  if (cudaMemset(plan->d_status, 0, sizeof(int)) != cudaSuccess) return WSATTN_ERR_CUDA;
+  return WSATTN_ERR_TIMEOUT;
+}
+
+int wsattn_selftest_timeout(int limit_ms, int* status, void* stream) {
+  if (!status || limit_ms < 1 || limit_ms > 10000) return WSATTN_ERR_BAD_ARG;
+  int dev = 0, clk = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&clk, cudaDevAttrClockRate, dev) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  int* d = nullptr;
+  if (cudaMalloc(&d, sizeof(int)) != cudaSuccess) return WSATTN_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int rc = WSATTN_OK;
+  int st = -1;
+  if (cudaMemsetAsync(d, 0xFF, sizeof(int), s) != cudaSuccess ||
+      wsattn::launch_timeout_selftest(static_cast<long long>(limit_ms) * clk, d, s) !=
+          cudaSuccess ||
+      cudaMemcpyAsync(&st, d, sizeof(int), cudaMemcpyDeviceToHost, s) != cudaSuccess ||
+      cudaStreamSynchronize(s) != cudaSuccess)
+    rc = WSATTN_ERR_CUDA;
+  cudaFree(d);
+  if (rc == WSATTN_OK) *status = st == wsattn::kStatusTimeoutSelftest ? WSATTN_ERR_TIMEOUT
+                                 : st == 0                            ? WSATTN_OK
+                                                                      : WSATTN_ERR_CUDA;
+  return rc;
+}
+
+const char* wsattn_status_string(int status) {
+  switch (status) {
+    case WSATTN_OK: return "ok";
+    case WSATTN_ERR_BAD_ARG: return "bad argument";
+    case WSATTN_ERR_BAD_BLOCK: return "block size must be a multiple of 16 dividing tokens_per_frame";
+    case WSATTN_ERR_UNSUPPORTED: return "unsupported head_dim or block_k";
+    case WSATTN_ERR_NOT_PREPARED: return "forward called before prepare";
+    case WSATTN_ERR_BATCH_MISMATCH: return "batch differs from the last prepare";
+    case WSATTN_ERR_CUDA: return "CUDA runtime error";
+    case WSATTN_ERR_TIMEOUT: return "device-side wait expired";
+    case WSATTN_ERR_NO_MEMORY: return "host allocation failed";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

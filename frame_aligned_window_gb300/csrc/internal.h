@@ -1,0 +1,109 @@
+// Internal declarations shared by the translation units of libwsattn.
+#pragma once
+
+#include <cstdint>
+#include <vector>
+
+#include <cuda.h>
+#include <cuda_runtime.h>
+
+#include "wsattn.h"
+
+namespace wsattn {
+
+// Rows of one query tile: the M of every tcgen05.mma the forward issues.
+constexpr int kTileM = 128;
+// Largest key block the forward kernel streams (tensor-memory budget:
+// O (D cols) + two S buffers + Q (D/2 cols) within 512 columns).
+constexpr int kMaxBlockK = 160;
+// Default eligibility threshold, in scaled-logit units.
+constexpr float kDefaultTau = 40.0f;
+
+// One unit of forward work for one (b, h): a 128-row query tile inside one
+// frame and that frame's list of active key blocks.
+struct WorkTile {
+  int32_t row0;    // first query token of the tile (within the head)
+  int32_t nvalid;  // rows of the tile that belong to the frame (<= 128)
+  int32_t kbeg;    // [kbeg, kend) indexes the frame's key blocks in kcol
+  int32_t kend;
+};
+
+// Host-side plan: geometry, block map, and the forward work list.
+struct HostPlan {
+  int F = 0, T = 0, w = 0, R = 0, H = 0, D = 0, bq = 0, bk = 0;
+  int64_t N = 0, nqb = 0, nkb = 0;
+  std::vector<uint8_t> bitmap;     // [nqb * nkb]
+  std::vector<int32_t> row_ptr;    // [nqb + 1]
+  std::vector<int32_t> col;        // [nnz]
+  std::vector<WorkTile> tiles;     // longest first
+  std::vector<int32_t> kcol;       // per frame, key block indices (units of bk)
+  int64_t active_pairs = 0;        // active (query, key) pairs per (b, h)
+};
+
+// Builds everything above; returns a WSATTN_* status.
+int build_host_plan(int frames, int tokens_per_frame, int window, int ref_frames, int heads,
+                    int head_dim, int block_q, int block_k, HostPlan* out);
+
+// Picks a block size for T: the largest valid size <= 128 if it is >= 48,
+// else the largest valid size <= 160 (valid: multiple of 16 dividing T).
+int auto_block(int T);
+
+// ------------------------------------------------------------ prepare
+struct PrepBuffers {
+  float* b_rows;        // [BH * N] bound b_i; holds ||q_i|| between passes
+  float* m_rows;        // [BH * N] fixed max m_i = b_i + scale q_i.mu; holds c_i between passes
+  float* mu;            // [BH * D]
+  float* kmax;          // [BH]
+  float* bmax;          // [BH]
+  uint8_t* elig;        // [BH]
+  float* part_sum;      // [BH * nchunk * D]
+  float* part_kmax;     // [BH * nchunk]
+  float* part_qmax;     // [BH * nchunk]
+  int nchunk;
+  int rows_per_chunk;
+};
+
+// Enqueues the three prepare passes; returns a cudaError_t.
+cudaError_t launch_prepare(const void* q, const void* k, int BH, int64_t N, int D, float scale,
+                           float tau, const PrepBuffers& buf, cudaStream_t stream);
+
+// Chunking of the N rows of one head across CTAs.
+void prepare_chunking(int BH, int64_t N, int num_sms, int* nchunk, int* rows_per_chunk);
+
+// ------------------------------------------------------------ forward
+struct FwdParams {
+  CUtensorMap tm_q;  // [BH*N, D] bf16, box {64, 128}, 128-byte swizzle
+  CUtensorMap tm_k;  // [BH*N, D] bf16, box {64, bk}
+  CUtensorMap tm_v;  // [BH*N, D] bf16, box {64, bk}
+  const WorkTile* tiles;
+  const int32_t* kcol;
+  const float* m_rows;   // [BH*N] fixed softmax max per row (uncentered logit units)
+  const uint8_t* elig;   // [BH]
+  float* out;            // [BH*N, D]
+  int* status;           // device status word (bit set on an expired wait)
+  int n_tiles;           // work tiles per (b, h)
+  int bh;                // batch * heads
+  int n;                 // tokens per head
+  int bk;                // key block rows
+  int stages_k, stages_v;
+  int force_path;        // -1 auto, 0 fixed, 1 online
+  float scale_log2;      // softmax scale * log2(e)
+};
+
+// Dynamic shared memory the forward kernel needs for (D, bk, stages).
+size_t forward_smem_bytes(int D, int bk, int stages_k, int stages_v);
+// Largest stage counts (<= 4 each) that fit the per-block shared memory.
+void forward_stages(int D, int bk, size_t smem_optin, int* stages_k, int* stages_v);
+// Launches the persistent forward kernel on `grid` CTAs.
+cudaError_t launch_forward(const FwdParams& p, int D, int grid, size_t smem, cudaStream_t s);
+
+// Self test of the bounded wait (see wsattn_selftest_timeout).
+cudaError_t launch_timeout_selftest(long long limit_cycles, int* status, cudaStream_t s);
+
+// Device status bits.
+constexpr int kStatusTimeoutProducer = 1;
+constexpr int kStatusTimeoutMma = 2;
+constexpr int kStatusTimeoutSoftmax = 4;
+constexpr int kStatusTimeoutSelftest = 8;
+
+}  // namespace wsattn

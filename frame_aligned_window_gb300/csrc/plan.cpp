@@ -1,0 +1,114 @@
+// Block-map builder (host only).
+//
+// Google Developers Blog post "HeyGen x Google Cloud: Bringing Avatar IV to
+// TPUs", section "Deleting the mask" (Fig. 3): the mask is frame-aligned, so
+// with block sizes that are multiples of 16 and divide the frame token span T
+// every block lies inside one query frame and one key frame and is therefore
+// entirely active or entirely skipped.  The map is built at frame granularity
+// and expanded to blocks; no element of the mask is ever materialised.
+//
+// Frame rule (token-order frame indices; reference frames are the prefix):
+// query frame a sees key frame c iff c is a reference frame, a is a reference
+// frame (reference queries are global), or |(a - R) - (c - R)| <= w.
+#include <algorithm>
+#include <new>
+
+#include "internal.h"
+
+namespace wsattn {
+
+static bool valid_block(int b, int T) { return b >= 16 && b % 16 == 0 && T % b == 0; }
+
+int auto_block(int T) {
+  int best128 = 0, best_max = 0;
+  for (int b = 16; b <= kMaxBlockK && b <= T; b += 16) {
+    if (T % b != 0) continue;
+    if (b <= 128) best128 = b;
+    best_max = b;
+  }
+  return best128 >= 48 ? best128 : best_max;
+}
+
+static bool frames_interact(int a, int c, int w, int R) {
+  if (c < R || a < R) return true;
+  int d = a - c;
+  if (d < 0) d = -d;
+  return d <= w;
+}
+
+int build_host_plan(int frames, int tokens_per_frame, int window, int ref_frames, int heads,
+                    int head_dim, int block_q, int block_k, HostPlan* out) {
+  if (!out) return WSATTN_ERR_BAD_ARG;
+  if (frames < 1 || ref_frames < 0 || window < 0 || heads < 1) return WSATTN_ERR_BAD_ARG;
+  if (tokens_per_frame < 16 || tokens_per_frame % 16 != 0) return WSATTN_ERR_BAD_BLOCK;
+  if (head_dim != 64 && head_dim != 128) return WSATTN_ERR_UNSUPPORTED;
+  const int T = tokens_per_frame;
+  const int64_t nf = static_cast<int64_t>(frames) + ref_frames;
+  const int64_t N = nf * T;
+  // Query rows and key coordinates are int32 inside the kernels.
+  if (N > (int64_t(1) << 30)) return WSATTN_ERR_BAD_ARG;
+  const int bq = block_q ? block_q : auto_block(T);
+  const int bk = block_k ? block_k : auto_block(T);
+  if (block_q < 0 || block_k < 0) return WSATTN_ERR_BAD_BLOCK;
+  if (!valid_block(bq, T) || !valid_block(bk, T)) return WSATTN_ERR_BAD_BLOCK;
+
+  HostPlan& p = *out;
+  p = HostPlan{};
+  p.F = frames; p.T = T; p.w = window; p.R = ref_frames; p.H = heads; p.D = head_dim;
+  p.bq = bq; p.bk = bk; p.N = N;
+  p.nqb = N / bq;
+  p.nkb = N / bk;
+  try {
+    // Bitmap and CSR.
+    p.bitmap.assign(static_cast<size_t>(p.nqb * p.nkb), 0);
+    p.row_ptr.assign(static_cast<size_t>(p.nqb + 1), 0);
+    for (int64_t qb = 0; qb < p.nqb; ++qb) {
+      const int a = static_cast<int>(qb * bq / T);
+      for (int64_t kb = 0; kb < p.nkb; ++kb) {
+        const int c = static_cast<int>(kb * bk / T);
+        if (frames_interact(a, c, window, ref_frames)) {
+          p.bitmap[static_cast<size_t>(qb * p.nkb + kb)] = 1;
+          p.col.push_back(static_cast<int32_t>(kb));
+        }
+      }
+      p.row_ptr[static_cast<size_t>(qb + 1)] = static_cast<int32_t>(p.col.size());
+    }
+    // Active element pairs per (b, h): T*T per interacting frame pair.
+    int64_t pairs = 0;
+    for (int64_t a = 0; a < nf; ++a)
+      for (int64_t c = 0; c < nf; ++c)
+        if (frames_interact(static_cast<int>(a), static_cast<int>(c), window, ref_frames)) pairs++;
+    p.active_pairs = pairs * T * T;
+
+    // Work list: every 128-row query tile of every frame, with the frame's key
+    // blocks.  The key list of frame a is the CSR row of its first q-block
+    // (all q-blocks of a frame share it).
+    const int tiles_per_frame = (T + kTileM - 1) / kTileM;
+    for (int64_t a = 0; a < nf; ++a) {
+      const int64_t qb0 = a * T / bq;
+      const int32_t kbeg = static_cast<int32_t>(p.kcol.size());
+      for (int32_t e = p.row_ptr[static_cast<size_t>(qb0)];
+           e < p.row_ptr[static_cast<size_t>(qb0 + 1)]; ++e)
+        p.kcol.push_back(p.col[static_cast<size_t>(e)]);
+      const int32_t kend = static_cast<int32_t>(p.kcol.size());
+      for (int t = 0; t < tiles_per_frame; ++t) {
+        WorkTile wt;
+        wt.row0 = static_cast<int32_t>(a * T + t * kTileM);
+        wt.nvalid = std::min(kTileM, T - t * kTileM);
+        wt.kbeg = kbeg;
+        wt.kend = kend;
+        p.tiles.push_back(wt);
+      }
+    }
+    // Longest first (the reference frame's tiles see every key block); the
+    // order among equal lengths stays the token order.
+    std::stable_sort(p.tiles.begin(), p.tiles.end(), [](const WorkTile& x, const WorkTile& y) {
+      return (x.kend - x.kbeg) > (y.kend - y.kbeg);
+    });
+  } catch (const std::bad_alloc&) {
+    return WSATTN_ERR_NO_MEMORY;
+  }
+  return WSATTN_OK;
+}
+
+}  // namespace wsattn

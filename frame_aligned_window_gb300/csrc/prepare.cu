@@ -1,0 +1,236 @@
+// Fixed-max statistics: key mean, Cauchy-Schwarz row bounds and per-head
+// eligibility.
+//
+// Google Developers Blog post "HeyGen x Google Cloud: Bringing Avatar IV to
+// TPUs", section "Breaking softmax's dependency chain": a query's largest
+// logit is at most its norm times the largest key norm; centering the keys
+// on their shared mean first tightens that bound and leaves the softmax
+// unchanged; a head whose bound is too loose (its exponentials would
+// underflow) takes the online path.  The small per-row arrays this produces
+// are what the forward kernel reads at the start of each query tile.
+//
+// The centering is applied to the bound, not to the stored keys: with
+//   s'_ij = scale q_i.(k_j - mu) = s_ij - c_i,   c_i = scale q_i.mu,
+// the fixed-max probability exp(s'_ij - b_i) equals exp(s_ij - m_i) with
+// m_i = b_i + c_i.  The forward kernel multiplies the caller's bf16 keys as
+// they are (no second rounding of k - mu) and uses m_i as the row's fixed max.
+//
+// Three HBM-bound passes over [BH, N, D] bf16, each CTA owning one chunk of
+// rows of one (b, h); every reduction runs in a fixed order (no atomics), so
+// the results are bit-reproducible:
+//   A  per-chunk key column sums                                (reads k)
+//   B  mu = ordered sum of the chunk sums / N; key norms ||k_j - mu|| and
+//      their per-chunk max; query norms ||q_i||, c_i, per-chunk max query
+//      norm (row norms reduced with warp shuffles)        (reads k and q)
+//   C  K_h = max of the chunk maxima; b_i = (scale ||q_i||) K_h;
+//      m_i = b_i + c_i; B_h = (scale max ||q_i||) K_h, which equals max_i b_i
+//      because the expression is monotone in ||q_i||;
+//      eligible = B_h <= tau and 2 B_h < 126 ln 2.
+#include <cuda_bf16.h>
+
+#include "internal.h"
+
+namespace wsattn {
+namespace {
+
+constexpr int kPrepThreads = 256;
+
+// Eight bf16 in a 16-byte word -> fp32 (exact: bf16 is the top half of fp32).
+__device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
+  const uint32_t w[4] = {u.x, u.y, u.z, u.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    f[2 * i] = __uint_as_float(w[i] << 16);
+    f[2 * i + 1] = __uint_as_float(w[i] & 0xFFFF0000u);
+  }
+}
+
+template <int kLanes>
+__device__ __forceinline__ float group_sum(float v) {
+#pragma unroll
+  for (int o = kLanes / 2; o > 0; o >>= 1) v += __shfl_xor_sync(0xffffffffu, v, o);
+  return v;
+}
+
+// Max over the CTA; the result is valid in thread 0.  Contains __syncthreads.
+__device__ __forceinline__ float block_max(float v, float* scratch) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) v = fmaxf(v, __shfl_xor_sync(0xffffffffu, v, o));
+  if ((threadIdx.x & 31) == 0) scratch[threadIdx.x / 32] = v;
+  __syncthreads();
+  float m = 0.f;
+  if (threadIdx.x == 0) {
+    for (int w = 0; w < kPrepThreads / 32; ++w) m = fmaxf(m, scratch[w]);
+  }
+  return m;
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPrepThreads)
+    prep_pass_a(const uint16_t* __restrict__ k, int64_t n, int rpc, int nchunk,
+                float* __restrict__ part_sum) {
+  constexpr int kLanes = D / 8;                 // threads sharing one row
+  constexpr int kRows = kPrepThreads / kLanes;  // rows in flight per CTA
+  __shared__ float red[kRows][D];
+  const int bh = blockIdx.y, c = blockIdx.x;
+  const int lr = threadIdx.x % kLanes, rs = threadIdx.x / kLanes;
+  const int64_t r0 = static_cast<int64_t>(c) * rpc;
+  const int64_t r1 = min(n, r0 + rpc);
+  const size_t base = static_cast<size_t>(bh) * n;
+  float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+  for (int64_t r = r0 + rs; r < r1; r += kRows) {
+    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(k + (base + r) * D) + lr);
+    float kf[8];
+    unpack8(kv, kf);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] += kf[i];
+  }
+#pragma unroll
+  for (int i = 0; i < 8; ++i) red[rs][lr * 8 + i] = acc[i];
+  __syncthreads();
+  if (threadIdx.x < D) {
+    float s = 0.f;
+    for (int g = 0; g < kRows; ++g) s += red[g][threadIdx.x];
+    part_sum[(static_cast<size_t>(bh) * nchunk + c) * D + threadIdx.x] = s;
+  }
+}
+
+template <int D>
+__global__ void __launch_bounds__(kPrepThreads)
+    prep_pass_b(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k, int64_t n, int rpc,
+                int nchunk, float scale, const float* __restrict__ part_sum,
+                float* __restrict__ mu_out, float* __restrict__ qn, float* __restrict__ crow,
+                float* __restrict__ part_kmax, float* __restrict__ part_qmax) {
+  constexpr int kLanes = D / 8;
+  constexpr int kRows = kPrepThreads / kLanes;
+  __shared__ float mu_s[D];
+  __shared__ float wmax[kPrepThreads / 32];
+  const int bh = blockIdx.y, c = blockIdx.x;
+  const int lr = threadIdx.x % kLanes, rs = threadIdx.x / kLanes;
+  if (threadIdx.x < D) {
+    float s = 0.f;
+    for (int cc = 0; cc < nchunk; ++cc)
+      s += part_sum[(static_cast<size_t>(bh) * nchunk + cc) * D + threadIdx.x];
+    const float m = s / static_cast<float>(n);
+    mu_s[threadIdx.x] = m;
+    if (c == 0) mu_out[static_cast<size_t>(bh) * D + threadIdx.x] = m;
+  }
+  __syncthreads();
+  float mloc[8];
+#pragma unroll
+  for (int i = 0; i < 8; ++i) mloc[i] = mu_s[lr * 8 + i];
+  const int64_t r0 = static_cast<int64_t>(c) * rpc;
+  const int64_t r1 = min(n, r0 + rpc);
+  const size_t base = static_cast<size_t>(bh) * n;
+  float km = 0.f, qm = 0.f;
+  for (int64_t rb = r0; rb < r1; rb += kRows) {  // uniform trip count per warp
+    const int64_t r = rb + rs;
+    float kss = 0.f, qss = 0.f, qmu = 0.f;
+    if (r < r1) {
+      const uint4 kv = __ldg(reinterpret_cast<const uint4*>(k + (base + r) * D) + lr);
+      const uint4 qv = __ldg(reinterpret_cast<const uint4*>(q + (base + r) * D) + lr);
+      float kf[8], qf[8];
+      unpack8(kv, kf);
+      unpack8(qv, qf);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const float x = kf[i] - mloc[i];
+        kss = fmaf(x, x, kss);
+        qss = fmaf(qf[i], qf[i], qss);
+        qmu = fmaf(qf[i], mloc[i], qmu);
+      }
+    }
+    kss = group_sum<kLanes>(kss);
+    qss = group_sum<kLanes>(qss);
+    qmu = group_sum<kLanes>(qmu);
+    const float qnorm = sqrtf(qss);
+    if (r < r1 && lr == 0) {
+      qn[base + r] = qnorm;
+      crow[base + r] = scale * qmu;
+    }
+    km = fmaxf(km, sqrtf(kss));
+    qm = fmaxf(qm, qnorm);
+  }
+  const float kmb = block_max(km, wmax);
+  __syncthreads();  // wmax is reused
+  const float qmb = block_max(qm, wmax);
+  if (threadIdx.x == 0) {
+    part_kmax[static_cast<size_t>(bh) * nchunk + c] = kmb;
+    part_qmax[static_cast<size_t>(bh) * nchunk + c] = qmb;
+  }
+}
+
+__global__ void __launch_bounds__(kPrepThreads)
+    prep_pass_c(int64_t n, int rpc, int nchunk, float scale, float tau, float* __restrict__ b_rows,
+                float* __restrict__ m_rows, const float* __restrict__ part_kmax,
+                const float* __restrict__ part_qmax, float* __restrict__ kmax,
+                float* __restrict__ bmax, uint8_t* __restrict__ elig) {
+  __shared__ float k_s;
+  const int bh = blockIdx.y, c = blockIdx.x;
+  if (threadIdx.x == 0) {
+    float kh = 0.f;
+    for (int cc = 0; cc < nchunk; ++cc)
+      kh = fmaxf(kh, part_kmax[static_cast<size_t>(bh) * nchunk + cc]);
+    k_s = kh;
+  }
+  __syncthreads();
+  const float kh = k_s;
+  const int64_t r0 = static_cast<int64_t>(c) * rpc;
+  const int64_t r1 = min(n, r0 + rpc);
+  const size_t base = static_cast<size_t>(bh) * n;
+  for (int64_t r = r0 + threadIdx.x; r < r1; r += kPrepThreads) {
+    const float b = (scale * b_rows[base + r]) * kh;  // b_rows holds ||q_i|| here
+    b_rows[base + r] = b;
+    m_rows[base + r] = b + m_rows[base + r];          // m_rows holds c_i here
+  }
+  if (c == 0 && threadIdx.x == 0) {
+    float qm = 0.f;
+    for (int cc = 0; cc < nchunk; ++cc)
+      qm = fmaxf(qm, part_qmax[static_cast<size_t>(bh) * nchunk + cc]);
+    const float bm = (scale * qm) * kh;
+    const float underflow_limit = 126.0f * 0.693147180559945309f;
+    kmax[bh] = kh;
+    bmax[bh] = bm;
+    elig[bh] = static_cast<uint8_t>(bm <= tau && 2.0f * bm < underflow_limit);
+  }
+}
+
+}  // namespace
+
+void prepare_chunking(int BH, int64_t N, int num_sms, int* nchunk, int* rows_per_chunk) {
+  // About four waves of CTAs over the GPU, at least 64 rows per CTA.
+  int64_t want = (4LL * num_sms + BH - 1) / BH;
+  int64_t max_chunks = (N + 63) / 64;
+  if (want > max_chunks) want = max_chunks;
+  if (want < 1) want = 1;
+  int64_t rpc = (N + want - 1) / want;
+  rpc = (rpc + 15) / 16 * 16;
+  *rows_per_chunk = static_cast<int>(rpc);
+  *nchunk = static_cast<int>((N + rpc - 1) / rpc);
+}
+
+cudaError_t launch_prepare(const void* q, const void* k, int BH, int64_t N, int D, float scale,
+                           float tau, const PrepBuffers& b, cudaStream_t stream) {
+  const dim3 grid(b.nchunk, BH);
+  const uint16_t* q16 = static_cast<const uint16_t*>(q);
+  const uint16_t* k16 = static_cast<const uint16_t*>(k);
+  if (D == 128) {
+    prep_pass_a<128><<<grid, kPrepThreads, 0, stream>>>(k16, N, b.rows_per_chunk, b.nchunk,
+                                                        b.part_sum);
+    prep_pass_b<128><<<grid, kPrepThreads, 0, stream>>>(
+        q16, k16, N, b.rows_per_chunk, b.nchunk, scale, b.part_sum, b.mu, b.b_rows, b.m_rows,
+        b.part_kmax, b.part_qmax);
+  } else {
+    prep_pass_a<64><<<grid, kPrepThreads, 0, stream>>>(k16, N, b.rows_per_chunk, b.nchunk,
+                                                       b.part_sum);
+    prep_pass_b<64><<<grid, kPrepThreads, 0, stream>>>(
+        q16, k16, N, b.rows_per_chunk, b.nchunk, scale, b.part_sum, b.mu, b.b_rows, b.m_rows,
+        b.part_kmax, b.part_qmax);
+  }
+  prep_pass_c<<<grid, kPrepThreads, 0, stream>>>(N, b.rows_per_chunk, b.nchunk, scale, tau,
+                                                 b.b_rows, b.m_rows, b.part_kmax, b.part_qmax,
+                                                 b.kmax, b.bmax, b.elig);
+  return cudaGetLastError();
+}
+
+}  // namespace wsattn

@@ -1,0 +1,181 @@
+/*
+ * wsattn.h - C ABI of libwsattn: frame-aligned window-sparse attention for
+ * NVIDIA GB300 (sm_103a).
+ *
+ * The method is the one the Google Developers Blog post "HeyGen x Google
+ * Cloud: Bringing Avatar IV to TPUs" describes for the super-resolution
+ * stage's sparse attention:
+ *   - section "Deleting the mask" (Fig. 3): every frame's tokens attend a
+ *     window of nearby frames plus one global reference frame; with block
+ *     sizes that are multiples of 16 and divide the frame token span, every
+ *     key block is either fully active or skipped, so the kernel needs no
+ *     mask predicate, no padding and no second pass for the reference frame;
+ *   - section "Breaking softmax's dependency chain" (Fig. 4): keys are
+ *     mean-centered, each query row gets a Cauchy-Schwarz upper bound on its
+ *     logits (its norm times the max key norm) that serves as a fixed softmax
+ *     max, and heads whose bound is too loose fall back to the online-max
+ *     path inside the same kernel.
+ *
+ * Conventions shared by every call
+ *   - Token order: the R reference frames first, then video frames 0..F-1,
+ *     each T tokens long; N = (R + F) * T.  Query token i attends key token j
+ *     iff j lies in a reference frame, or i lies in a reference frame, or
+ *     their video frames differ by at most `window`.
+ *   - Tensors are row-major [batch, heads, N, head_dim], contiguous, in
+ *     device memory owned by the caller, with 16-byte aligned base pointers.
+ *     q, k, v are bf16 (passed as void*); out is fp32.
+ *   - softmax scale = 1 / sqrt(head_dim).
+ *   - `stream` is a cudaStream_t (NULL = legacy default stream); all device
+ *     work is enqueued on it.  No call synchronises the host except the
+ *     wsattn_get_* readers and wsattn_device_status, which say so.
+ *   - Every call returns a status code (WSATTN_OK = 0 or one of the errors
+ *     below) and never throws or aborts.  Argument errors are reported before
+ *     any work is enqueued.  Asynchronous device errors (CUDA faults, expired
+ *     device-side waits) surface through wsattn_device_status or the next
+ *     synchronising call.
+ *   - A plan is not thread-safe; calls on one plan must be serialised by the
+ *     caller.  Device buffers a plan owns live on the device that was current
+ *     at its first device call.
+ */
+#ifndef WSATTN_H_
+#define WSATTN_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+enum wsattn_status {
+  WSATTN_OK = 0,
+  WSATTN_ERR_BAD_ARG = 1,        /* null/misaligned pointer, size out of range */
+  WSATTN_ERR_BAD_BLOCK = 2,      /* block size not a multiple of 16 or not dividing T */
+  WSATTN_ERR_UNSUPPORTED = 3,    /* head_dim or block_k outside what the kernels implement */
+  WSATTN_ERR_NOT_PREPARED = 4,   /* wsattn_forward before any wsattn_prepare on the plan */
+  WSATTN_ERR_BATCH_MISMATCH = 5, /* forward batch differs from the last prepare's */
+  WSATTN_ERR_CUDA = 6,           /* a CUDA runtime call failed (launch, copy, alloc) */
+  WSATTN_ERR_TIMEOUT = 7,        /* a device-side wait expired; results are invalid */
+  WSATTN_ERR_NO_MEMORY = 8       /* host allocation failed */
+};
+
+typedef struct wsattn_plan_s* wsattn_plan_t;
+
+/*
+ * Builds the block map for one attention shape ("Deleting the mask", Fig. 3).
+ * Host-only: allocates no device memory and needs no GPU.
+ *   frames            F >= 1 video frames
+ *   tokens_per_frame  T >= 16, a multiple of 16
+ *   window            w >= 0; w >= F - 1 makes the mask dense
+ *   ref_frames        R >= 0 global reference frames (prefix of the sequence)
+ *   heads             H >= 1
+ *   head_dim          D; the kernels implement 64 and 128
+ *   block_q, block_k  block sizes of the map: multiples of 16 dividing T, or
+ *                     0 to let the plan choose (the largest valid size <= 128
+ *                     if it is >= 48, else the largest valid size <= 160).
+ *                     The forward kernel streams keys in block_k rows, so
+ *                     block_k must be <= 160 for wsattn_forward.
+ *   out               receives the plan handle (owned by the caller; release
+ *                     with wsattn_plan_destroy).
+ * Errors: BAD_ARG (sizes, null out), BAD_BLOCK, UNSUPPORTED (head_dim),
+ *         NO_MEMORY.
+ */
+int wsattn_plan(int frames, int tokens_per_frame, int window, int ref_frames, int heads,
+                int head_dim, int block_q, int block_k, wsattn_plan_t* out);
+
+/* Releases the plan and every host and device buffer it owns.  The caller
+ * must make sure no work that uses the plan is still running on the GPU.
+ * NULL is accepted and ignored. */
+int wsattn_plan_destroy(wsattn_plan_t plan);
+
+/*
+ * Fixed-max statistics ("Breaking softmax's dependency chain").  For every
+ * (b, h), with scale = 1/sqrt(D):
+ *   mu      = mean of the N keys (fp32, fixed reduction order);
+ *   K_h     = max_j ||k_j - mu||, the max norm of the centered keys;
+ *   b_i     = scale * ||q_i|| * K_h, row i's bound on its centered logits
+ *             scale * q_i.(k_j - mu) (Cauchy-Schwarz);
+ *   m_i     = b_i + scale * q_i.mu, the same bound on the logits of the keys
+ *             as given: centering shifts every logit of row i by the same
+ *             scale * q_i.mu, which the softmax does not see, so the forward
+ *             multiplies the caller's keys unchanged and uses m_i as the
+ *             row's fixed max;
+ *   B_h     = max_i b_i;  eligible_h = (B_h <= tau) and (2 * B_h < 126 ln 2),
+ *             tau = 40 unless overridden with wsattn_plan_set_debug.
+ * q and k are read only.  The statistics live in a workspace the plan owns
+ * (allocated on the first call, grown when batch grows; growing synchronises
+ * `stream`).
+ *   q  bf16 [batch, H, N, D]
+ *   k  bf16 [batch, H, N, D]
+ * Errors: BAD_ARG, CUDA.
+ */
+int wsattn_prepare(wsattn_plan_t plan, int batch, const void* q, const void* k, void* stream);
+
+/*
+ * out = masked softmax(q k^T * scale) v, computed in one pass over the
+ * plan's active key blocks by a persistent tcgen05 kernel: QK^T and PV on
+ * the tensor cores (bf16 inputs, fp32 accumulation in tensor memory), the
+ * row bound m_i as a fixed softmax max on eligible heads, the online max on
+ * the others.  P is rounded to bf16 for the PV product ("Proving pixels
+ * unchanged" moves the final attention matmul to bf16).
+ *   q    bf16 [batch, H, N, D]
+ *   k    bf16 [batch, H, N, D], the same keys wsattn_prepare saw
+ *   v    bf16 [batch, H, N, D]
+ *   out  fp32 [batch, H, N, D], fully overwritten
+ * Requires a prior wsattn_prepare on this plan with the same batch.
+ * Errors: BAD_ARG, NOT_PREPARED, BATCH_MISMATCH, UNSUPPORTED (block_k > 160),
+ *         CUDA.
+ */
+int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, const void* v,
+                   float* out, void* stream);
+
+/* ---------------------------------------------------------- introspection */
+
+/* Plan geometry.  info[0..9] = N, block_q, block_k, q blocks, k blocks,
+ * active blocks (CSR nnz), work tiles per (b, h) (128-row query tiles),
+ * head_dim, heads, active (query, key) element pairs per (b, h).  n is the
+ * capacity of info; at most n entries are written. */
+int wsattn_plan_info(wsattn_plan_t plan, int64_t* info, int n);
+
+/* Copies the block bitmap (row-major [N/block_q, N/block_k], 1 = active)
+ * into host memory of n bytes.  Errors: BAD_ARG if n is too small. */
+int wsattn_get_block_map(wsattn_plan_t plan, uint8_t* host, size_t n);
+
+/* Copies the CSR of active blocks: row_ptr[N/block_q + 1], col[nnz] (key
+ * block indices, increasing within a row), into host arrays of the given
+ * capacities.  Errors: BAD_ARG if a capacity is too small. */
+int wsattn_get_csr(wsattn_plan_t plan, int32_t* row_ptr, int32_t* col, size_t n_row_ptr,
+                   size_t n_col);
+
+/* Synchronises `stream`, then copies the statistics of the last prepare to
+ * host memory: b_rows fp32 [batch*H*N] (b_i), m_rows fp32 [batch*H*N] (m_i),
+ * mu fp32 [batch*H*D], kmax fp32 [batch*H] (K_h), bmax fp32 [batch*H] (B_h),
+ * elig uint8 [batch*H].  Any pointer may be NULL to skip it.
+ * Errors: NOT_PREPARED, CUDA. */
+int wsattn_get_stats(wsattn_plan_t plan, float* b_rows, float* m_rows, float* mu, float* kmax,
+                     float* bmax, uint8_t* elig, void* stream);
+
+/* Test hook.  force_path: -1 = per-head eligibility (default), 0 = fixed max
+ * on every head, 1 = online max on every head.  tau > 0 replaces the
+ * eligibility threshold used by later prepares (40 by default). */
+int wsattn_plan_set_debug(wsattn_plan_t plan, int force_path, float tau);
+
+/* Synchronises `stream` and reports the plan's device status word: OK, or
+ * TIMEOUT if a device-side wait of a kernel launched with this plan expired
+ * (the word is then cleared).  CUDA if the synchronisation itself failed. */
+int wsattn_device_status(wsattn_plan_t plan, void* stream);
+
+/* Failure-path self test: launches a one-thread kernel that waits on a
+ * barrier nothing completes, with a wait limit of about `limit_ms`
+ * milliseconds, and reports the status the kernel wrote (TIMEOUT expected)
+ * in *status.  Synchronises `stream`.  Returns CUDA if the launch failed. */
+int wsattn_selftest_timeout(int limit_ms, int* status, void* stream);
+
+/* Static text for a status code. */
+const char* wsattn_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* WSATTN_H_ */

@@ -1,0 +1,142 @@
+"""The C ABI on the CPU: the library loads, exports every declared symbol, and
+its host-side plan (block map, CSR, work list geometry, argument checks) is
+bit-exact against the oracle's element-by-element classification."""
+import ctypes
+import itertools
+import os
+import re
+
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from workloads import WORKLOADS
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared_symbols():
+    with open(os.path.join(ROOT, "include", "wsattn.h")) as f:
+        text = f.read()
+    return sorted(set(re.findall(r"^(?:int|const char\*)\s+(wsattn_\w+)\(", text, re.M)))
+
+
+def test_library_exports_every_declared_symbol():
+    import frame_aligned_window_gb300 as fw
+    lib = ctypes.CDLL(fw.LIB_PATH)
+    declared = _declared_symbols()
+    assert len(declared) >= 12
+    assert set(declared) == set(fw.EXPORTS)
+    for name in declared:
+        assert hasattr(lib, name), name
+
+
+def test_status_strings():
+    import frame_aligned_window_gb300 as fw
+    for code in range(9):
+        assert fw.wsattn_status_string(code) and fw.wsattn_status_string(code) != "unknown status"
+    assert fw.wsattn_status_string(99) == "unknown status"
+
+
+def valid_blocks(T, cap=None):
+    return [b for b in range(16, (cap or T) + 1, 16) if T % b == 0]
+
+
+def _plan_vs_oracle(F, T, w, R, bq, bk):
+    import frame_aligned_window_gb300 as fw
+    plan = fw.wsattn_plan(F, T, w, R, 2, 128, bq, bk)
+    want = oracle.blockmap(F, T, w, R, bq, bk)
+    assert want["partial"] == 0
+    np.testing.assert_array_equal(fw.wsattn_get_block_map(plan), want["bitmap"])
+    rp, col = fw.wsattn_get_csr(plan)
+    np.testing.assert_array_equal(rp, want["row_ptr"])
+    np.testing.assert_array_equal(col, want["col"])
+    assert plan.nnz == want["nnz"]
+    m_pairs = oracle.blockmap(F, T, w, R, T, T)["nnz"] * T * T
+    assert plan.active_pairs == m_pairs
+    assert plan.tiles_per_head == (F + R) * ((T + 127) // 128)
+    plan.destroy()
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_plan_matches_oracle_all_valid_sizes(name):
+    wl = WORKLOADS[name]
+    T = wl.tokens_per_frame
+    for bq, bk in itertools.product(valid_blocks(T), valid_blocks(T)):
+        _plan_vs_oracle(wl.frames, T, wl.window, wl.ref_frames, bq, bk)
+
+
+@pytest.mark.parametrize("bq,bk", [(80, 80), (16, 208), (1040, 80), (208, 16)])
+def test_plan_matches_oracle_sr_shaped(bq, bk):
+    wl = WORKLOADS["sr"]
+    _plan_vs_oracle(wl.frames, wl.tokens_per_frame, wl.window, wl.ref_frames, bq, bk)
+
+
+@pytest.mark.parametrize("case", [
+    (1, 16, 0, 0, 16, 16), (3, 32, 0, 2, 16, 32), (6, 48, 10, 1, 48, 16), (5, 64, 1, 0, 32, 64),
+    (2, 160, 1, 1, 160, 160),
+])
+def test_plan_matches_oracle_edge_shapes(case):
+    _plan_vs_oracle(*case)
+
+
+def test_auto_block_sizes():
+    import frame_aligned_window_gb300 as fw
+    expect = {"tiny": 48, "small": 16, "sr": 80, "sr_long": 80, "dense": 112}
+    for name, bk in expect.items():
+        wl = WORKLOADS[name]
+        plan = fw.wsattn_plan(wl.frames, wl.tokens_per_frame, wl.window, wl.ref_frames,
+                              wl.heads, wl.head_dim)
+        assert (plan.block_q, plan.block_k) == (bk, bk), name
+        assert plan.n_tokens == wl.n_tokens
+
+
+def test_plan_errors():
+    import frame_aligned_window_gb300 as fw
+    bad = [
+        ((0, 48, 1, 1, 2, 64, 0, 0), 1),     # no frames
+        ((4, 48, -1, 1, 2, 64, 0, 0), 1),    # negative window
+        ((4, 48, 1, -1, 2, 64, 0, 0), 1),    # negative ref frames
+        ((4, 48, 1, 1, 0, 64, 0, 0), 1),     # no heads
+        ((4, 40, 1, 1, 2, 64, 0, 0), 2),     # T not a multiple of 16
+        ((4, 48, 1, 1, 2, 64, 32, 0), 2),    # 32 does not divide 48
+        ((4, 48, 1, 1, 2, 64, 0, 24), 2),    # not a multiple of 16
+        ((4, 48, 1, 1, 2, 96, 0, 0), 3),     # head_dim
+    ]
+    for args, code in bad:
+        with pytest.raises(fw.WsattnError) as e:
+            fw.wsattn_plan(*args)
+        assert e.value.code == code, args
+    h = ctypes.c_void_p()
+    assert fw.raw_call("wsattn_plan")(4, 48, 1, 1, 2, 64, 0, 0, None) == 1
+    assert fw.raw_call("wsattn_plan")(4, 48, 1, 1, 2, 64, 0, 0, ctypes.byref(h)) == 0
+    assert fw.raw_call("wsattn_plan_destroy")(h) == 0
+    assert fw.raw_call("wsattn_plan_destroy")(None) == 0
+
+
+def test_call_order_errors_without_device_work():
+    import frame_aligned_window_gb300 as fw
+    plan = fw.wsattn_plan(4, 48, 1, 1, 2, 64)
+    fwd = fw.raw_call("wsattn_forward")
+    dummy = ctypes.c_void_p(1 << 20)  # aligned, never dereferenced: the checks come first
+    assert fwd(plan.handle, 1, dummy, dummy, dummy, dummy, None) == 4   # NOT_PREPARED
+    assert fwd(plan.handle, 0, dummy, dummy, dummy, dummy, None) == 1   # batch 0
+    assert fwd(plan.handle, 1, None, dummy, dummy, dummy, None) == 1    # null q
+    prep = fw.raw_call("wsattn_prepare")
+    assert prep(plan.handle, 0, dummy, dummy, None) == 1
+    assert prep(plan.handle, 1, ctypes.c_void_p((1 << 20) + 2), dummy, None) == 1  # misaligned
+    stats = fw.raw_call("wsattn_get_stats")
+    assert stats(plan.handle, None, None, None, None, None, None, None) == 4
+    assert fw.raw_call("wsattn_plan_set_debug")(plan.handle, 2, ctypes.c_float(0.0)) == 1
+    assert fw.raw_call("wsattn_device_status")(plan.handle, None) == 0  # no device work yet
+    small = (ctypes.c_uint8 * 4)()
+    assert fw.raw_call("wsattn_get_block_map")(plan.handle, small, 4) == 1
+
+
+@pytest.mark.skipif(torch.cuda.is_available(), reason="checks the no-GPU failure path")
+def test_prepare_without_gpu_fails_loudly():
+    import frame_aligned_window_gb300 as fw
+    plan = fw.wsattn_plan(4, 48, 1, 1, 2, 64)
+    dummy = ctypes.c_void_p(1 << 20)
+    assert fw.raw_call("wsattn_prepare")(plan.handle, 1, dummy, dummy, None) == 6  # CUDA

@@ -1,0 +1,189 @@
+"""Forward kernel vs the oracle (GPU), through the C ABI.
+
+Bar: fp32 outputs from bf16 inputs within max-abs 1e-2 and relative L2
+5e-3 of the oracle's fp64 masked softmax attention (which uses the original,
+uncentered keys).  tiny and small are compared on every row; the SR-shaped,
+SR-long and dense workloads run at full size in the bench's launch
+configuration and are compared on sampled rows (frame-edge rows of every
+frame plus seeded random rows) of sampled heads, with properties that hold
+for every row checked on the whole output.
+"""
+import numpy as np
+import pytest
+import torch
+
+from _helpers import TOL_MAX_ABS, TOL_REL_L2, flat_heads, gpu_run, oracle_rows, rel_l2, workload
+import oracle
+from workloads import Workload, generate, micro, sample_heads, sample_rows
+
+pytestmark = pytest.mark.gpu
+
+
+def _check(got, want, what=""):
+    diff = np.abs(got - want)
+    err = float(diff.max())
+    rl2 = rel_l2(got, want)
+    where = np.unravel_index(int(diff.argmax()), diff.shape)
+    assert err <= TOL_MAX_ABS and rl2 <= TOL_REL_L2, \
+        f"{what}: max_abs={err:.3e} at {where} rel_l2={rl2:.3e}"
+    return err, rl2
+
+
+def _full_compare(wl, q, k, v, out):
+    want = oracle.attention_full(q, k, v, wl.frames, wl.tokens_per_frame, wl.window,
+                                 wl.ref_frames, wl.scale)
+    got = flat_heads(out.cpu(), wl).double().numpy()
+    return _check(got, want, wl.name)
+
+
+@pytest.mark.parametrize("name", ["tiny", "small"])
+def test_forward_full_parity(name):
+    wl = workload(name)
+    q, k, v = generate(wl)
+    _, out, _ = gpu_run(wl, q, k, v)
+    _full_compare(wl, q, k, v, out)
+
+
+def _sampled_compare(wl, q, k, v, out):
+    bh_list = sample_heads(wl)
+    rows = sample_rows(wl)
+    want = oracle_rows(wl, q, k, v, bh_list, rows)
+    o = flat_heads(out, wl)
+    idx = torch.tensor([b * wl.heads + h for b, h in bh_list], device=out.device)
+    got = o[idx][:, torch.tensor(rows, device=out.device)].cpu().double().numpy()
+    return _check(got, want, wl.name)
+
+
+def _whole_output_properties(wl, out, v):
+    # every output row is a convex combination of value rows of its head
+    o = flat_heads(out, wl)
+    vv = flat_heads(v.to(out.device), wl).float()
+    assert torch.isfinite(o).all()
+    # P is rounded to bf16 while l sums the unrounded p, so the weights sum
+    # to 1 within 2^-9: allow that much of the largest |v| on either side
+    slack = 2.0 ** -8 * vv.abs().amax(dim=(1, 2), keepdim=True) + 1e-4
+    lo = vv.amin(dim=1, keepdim=True) - slack
+    hi = vv.amax(dim=1, keepdim=True) + slack
+    assert ((o >= lo) & (o <= hi)).all()
+
+
+@pytest.mark.parametrize("name", ["sr", "sr_long", "dense"])
+def test_forward_full_size_sampled_parity(name):
+    wl = workload(name)
+    q, k, v = generate(wl)
+    plan, out, _ = gpu_run(wl, q, k, v)
+    _sampled_compare(wl, q, k, v, out)
+    _whole_output_properties(wl, out, v)
+
+
+def test_fallback_heads_take_online_path_and_paths_agree():
+    # SR-long: heads 5 and 17 are ineligible (bound above tau) and run the
+    # online max; forcing either path on every head gives the same result.
+    import frame_aligned_window_gb300 as fw
+    wl = workload("sr_long")
+    q, k, v = generate(wl)
+    plan, out_auto, _ = gpu_run(wl, q, k, v)
+    st = fw.wsattn_get_stats(plan, wl.batch)
+    assert [h for h in range(wl.heads) if st["elig"][h] == 0] == list(wl.boost_heads)
+    _, out_online, _ = gpu_run(wl, q, k, v, force_path=1)
+    normal = [h for h in range(wl.heads) if h not in wl.boost_heads]
+    a = out_auto[0, normal].float()
+    b = out_online[0, normal].float()
+    assert float((a - b).abs().max()) <= TOL_MAX_ABS
+    # on the ineligible heads the auto run IS the online path
+    assert torch.equal(out_auto[0, list(wl.boost_heads)], out_online[0, list(wl.boost_heads)])
+
+
+def test_forced_paths_agree_on_small():
+    wl = workload("small")
+    q, k, v = generate(wl)
+    _, fixed, _ = gpu_run(wl, q, k, v, force_path=0)
+    _, online, _ = gpu_run(wl, q, k, v, force_path=1)
+    _full_compare(wl, q, k, v, fixed)
+    _full_compare(wl, q, k, v, online)
+    assert float((fixed - online).abs().max()) <= TOL_MAX_ABS
+
+
+def test_forward_is_deterministic():
+    wl = workload("sr")
+    q, k, v = generate(wl)
+    _, a, _ = gpu_run(wl, q, k, v)
+    _, b, _ = gpu_run(wl, q, k, v)
+    assert torch.equal(a, b)
+
+
+@pytest.mark.parametrize("bk", [16, 48])
+def test_block_sizes_tiny(bk):
+    wl = workload("tiny")
+    q, k, v = generate(wl)
+    _, out, _ = gpu_run(wl, q, k, v, block_k=bk)
+    _full_compare(wl, q, k, v, out)
+
+
+@pytest.mark.parametrize("bk", [16, 80, 160])
+def test_block_sizes_sr_long_shape_small(bk):
+    # the SR-long frame span (T = 2080) with fewer frames and heads
+    wl, q, k, v = micro(41, 1, 2, 128, 4, 1, 2080, 1)
+    _, out, _ = gpu_run(wl, q, k, v, block_k=bk)
+    rows = sample_rows(wl, n_random=64)
+    want = oracle_rows(wl, q, k, v, [(0, 0), (0, 1)], rows)
+    got = flat_heads(out.cpu(), wl)[:, rows].double().numpy()
+    _check(got, want, f"bk={bk}")
+
+
+@pytest.mark.parametrize("case", [
+    # seed, B, H, D, F, R, T, w: edge shapes
+    (51, 1, 1, 128, 1, 0, 16, 0),      # one frame of 16 tokens (single block, ragged tile)
+    (52, 1, 2, 128, 5, 0, 48, 0),      # no reference frame, window 0
+    (53, 2, 3, 64, 3, 2, 160, 1),      # two reference frames, D=64, batch 2
+    (54, 1, 1, 128, 6, 1, 256, 10),    # window beyond the frame count (dense)
+    (55, 1, 2, 128, 3, 1, 144, 1),     # T = 128 + 16: a full tile and a 16-row tail
+])
+def test_edge_shapes_full_parity(case):
+    seed, B, H, D, F, R, T, w = case
+    wl, q, k, v = micro(seed, B, H, D, F, R, T, w)
+    _, out, _ = gpu_run(wl, q, k, v)
+    _full_compare(wl, q, k, v, out)
+
+
+def test_degenerate_inputs():
+    wl, q, k, v = micro(56, 1, 2, 128, 4, 1, 96, 1)
+    # zero queries: every row is the mean of the values it sees
+    qz = torch.zeros_like(q)
+    _, out, _ = gpu_run(wl, qz, k, v)
+    _full_compare(wl, qz, k, v, out)
+    # constant values come back unchanged
+    vc = torch.full_like(v, 0.75)
+    _, out, _ = gpu_run(wl, q, k, vc)
+    assert float((out - 0.75).abs().max()) <= 1e-2
+    # keys with no shared offset and large queries (online path on every head)
+    wl2, q2, k2, v2 = micro(57, 1, 2, 128, 4, 1, 96, 1, offset_std=0.0)
+    q2 = (q2.float() * 6).to(torch.bfloat16)
+    import frame_aligned_window_gb300 as fw
+    plan, out2, _ = gpu_run(wl2, q2, k2, v2)
+    st = fw.wsattn_get_stats(plan, 1)
+    assert not st["elig"].any()
+    _full_compare(wl2, q2, k2, v2, out2)
+
+
+def test_batch_mismatch_and_status():
+    import frame_aligned_window_gb300 as fw
+    wl, q, k, v = micro(58, 2, 2, 64, 3, 1, 48, 1)
+    plan = fw.wsattn_plan(wl.frames, wl.tokens_per_frame, wl.window, wl.ref_frames, wl.heads,
+                          wl.head_dim)
+    qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+    fw.wsattn_prepare(plan, qd, kd)
+    with pytest.raises(fw.WsattnError) as e:
+        fw.wsattn_forward(plan, qd[:1], kd[:1], vd[:1])
+    assert e.value.code == 5
+    fw.wsattn_forward(plan, qd, kd, vd)
+    assert fw.wsattn_device_status(plan) == 0
+
+
+def test_bounded_wait_reports_timeout():
+    # a kernel waits on a barrier nothing completes; the wait gives up after
+    # its limit and the status comes back to the host; the context stays usable
+    import frame_aligned_window_gb300 as fw
+    assert fw.wsattn_selftest_timeout(20) == 7
+    x = torch.ones(4, device="cuda")
+    assert float(x.sum()) == 4.0
