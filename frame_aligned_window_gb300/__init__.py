@@ -10,7 +10,7 @@ The names mirror the C ABI:
     wsattn_plan, wsattn_plan_destroy, wsattn_prepare, wsattn_forward,
     wsattn_plan_info, wsattn_get_block_map, wsattn_get_csr, wsattn_get_stats,
     wsattn_plan_set_debug, wsattn_device_status, wsattn_selftest_timeout,
-    wsattn_status_string
+    wsattn_status_string, wsattn_prepare_static
 """
 from __future__ import annotations
 
@@ -27,7 +27,7 @@ EXPORTS = (
     "wsattn_plan", "wsattn_plan_destroy", "wsattn_prepare", "wsattn_forward",
     "wsattn_plan_info", "wsattn_get_block_map", "wsattn_get_csr", "wsattn_get_stats",
     "wsattn_plan_set_debug", "wsattn_device_status", "wsattn_selftest_timeout",
-    "wsattn_status_string",
+    "wsattn_status_string", "wsattn_prepare_static",
 )
 
 STATUS = {0: "OK", 1: "BAD_ARG", 2: "BAD_BLOCK", 3: "UNSUPPORTED", 4: "NOT_PREPARED",
@@ -58,6 +58,7 @@ _lib.wsattn_plan_set_debug.argtypes = [_P, _I, _F]
 _lib.wsattn_device_status.argtypes = [_P, _P]
 _lib.wsattn_selftest_timeout.argtypes = [_I, ctypes.POINTER(_I), _P]
 _lib.wsattn_status_string.argtypes = [_I]
+_lib.wsattn_prepare_static.argtypes = [_I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P]
 _lib.wsattn_status_string.restype = ctypes.c_char_p
 for _name in EXPORTS:
     if _name != "wsattn_status_string":
@@ -222,6 +223,34 @@ def wsattn_selftest_timeout(limit_ms: int = 50, stream=None) -> int:
     _check(_lib.wsattn_selftest_timeout(int(limit_ms), ctypes.byref(st), _stream_ptr(stream)),
            "wsattn_selftest_timeout")
     return int(st.value)
+
+
+def wsattn_prepare_static(q, k, out: dict, tau: float = 40.0, stream=None):
+    """No-allocation prepare: statistics into the caller's tensors in `out`
+    (keys b, m, mu, kmax, bmax, elig, shaped as wsattn_prepare_static_outputs
+    makes them).  For callers that must not let the library allocate."""
+    import torch
+    B, H, N, D = q.shape
+    if k.shape != q.shape:
+        raise ValueError("q and k shapes differ")
+    _check(_lib.wsattn_prepare_static(
+        B, H, N, D, float(tau), _dev_ptr(q, "q", torch.bfloat16), _dev_ptr(k, "k", torch.bfloat16),
+        _dev_ptr(out["b"], "b", torch.float32), _dev_ptr(out["m"], "m", torch.float32),
+        _dev_ptr(out["mu"], "mu", torch.float32), _dev_ptr(out["kmax"], "kmax", torch.float32),
+        _dev_ptr(out["bmax"], "bmax", torch.float32), _dev_ptr(out["elig"], "elig", torch.uint8),
+        _stream_ptr(stream)), "wsattn_prepare_static")
+    return out
+
+
+def wsattn_prepare_static_outputs(batch, heads, n_tokens, head_dim, device="cuda"):
+    """Caller-owned output tensors for wsattn_prepare_static."""
+    import torch
+    bh = batch * heads
+    f = dict(dtype=torch.float32, device=device)
+    return {"b": torch.empty(bh, n_tokens, **f), "m": torch.empty(bh, n_tokens, **f),
+            "mu": torch.empty(bh, head_dim, **f), "kmax": torch.empty(bh, **f),
+            "bmax": torch.empty(bh, **f),
+            "elig": torch.empty(bh, dtype=torch.uint8, device=device)}
 
 
 def raw_call(name: str):

@@ -1,0 +1,128 @@
+// wsattn_prepare_static: the prepare statistics without any device
+// allocation.
+//
+// wsattn_prepare keeps its per-chunk partial sums in a workspace the plan
+// allocates with cudaMalloc.  Some callers cannot let a library do that: a
+// host framework that owns every byte of device memory through its own pool
+// or a fixed budget, or a latency-critical loop that cannot afford
+// cudaMalloc's implicit device synchronisation.  This entry point runs the
+// same three prepare kernels, writes the statistics into buffers the caller
+// passes in, and takes its scratch from a fixed array in the library's own
+// device image instead of allocating it.
+//
+// The scratch array, g_prepare_scratch below, holds kStaticSlots chunk slots
+// (a partial key-column sum of up to 128 floats plus two partial maxima per
+// slot): 2048 slots, 1,064,960 bytes.  Every GPU that loads the library holds
+// that memory until the process exits.
+//
+// Sharing rules:
+//   - every call uses the same array, and the array keeps whatever the last
+//     call left in it.  Nothing needs to start at zero: each pass writes every
+//     slot that a later pass of the same call reads;
+//   - calls whose kernels can overlap on the GPU (for example calls on two
+//     streams of one process with no event ordering them) race on the array
+//     and corrupt each other's results; callers must order such calls.  Each
+//     process has its own copy of the array;
+//   - the first call on a device looks up the array's device address (with
+//     that device current) and caches it; make that first call before any
+//     stream capture begins.
+#include <mutex>
+
+#include "internal.h"
+
+namespace wsattn {
+namespace {
+
+constexpr int kStaticSlots = 2048;
+constexpr int kStaticMaxDim = 128;
+constexpr size_t kStaticFloats =
+    static_cast<size_t>(kStaticSlots) * kStaticMaxDim + 2 * static_cast<size_t>(kStaticSlots);
+
+// Host code must not use this name as a device address: on the host it is a
+// stand-in object.  The device address comes from cudaGetSymbolAddress.
+static __device__ __align__(256) float g_prepare_scratch[kStaticFloats];
+
+constexpr int kMaxDevices = 64;
+std::mutex g_scratch_mu;
+float* g_scratch_ptr[kMaxDevices] = {};
+int g_num_sms[kMaxDevices] = {};
+
+// Device address of the scratch array and SM count for the current device,
+// looked up once per device.
+int scratch_for_current_device(float** ptr, int* num_sms) {
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return WSATTN_ERR_CUDA;
+  if (dev < 0 || dev >= kMaxDevices) return WSATTN_ERR_BAD_ARG;
+  std::lock_guard<std::mutex> lock(g_scratch_mu);
+  if (!g_scratch_ptr[dev]) {
+    void* p = nullptr;
+    if (cudaGetSymbolAddress(&p, g_prepare_scratch) != cudaSuccess || !p)
+      return WSATTN_ERR_CUDA;
+    int sms = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess)
+      return WSATTN_ERR_CUDA;
+    g_scratch_ptr[dev] = static_cast<float*>(p);
+    g_num_sms[dev] = sms;
+  }
+  *ptr = g_scratch_ptr[dev];
+  *num_sms = g_num_sms[dev];
+  return WSATTN_OK;
+}
+
+bool aligned(const void* p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) & (a - 1)) == 0; }
+
+}  // namespace
+}  // namespace wsattn
+
+extern "C" int wsattn_prepare_static(int batch, int heads, int n_tokens, int head_dim, float tau,
+                                     const void* q, const void* k, float* b_rows, float* m_rows,
+                                     float* mu, float* kmax, float* bmax, uint8_t* elig,
+                                     void* stream) {
+  using namespace wsattn;
+  if (batch < 1 || heads < 1 || n_tokens < 1 || !(tau > 0.0f)) return WSATTN_ERR_BAD_ARG;
+  if (head_dim != 64 && head_dim != 128) return WSATTN_ERR_UNSUPPORTED;
+  if (!q || !k || !b_rows || !m_rows || !mu || !kmax || !bmax || !elig) return WSATTN_ERR_BAD_ARG;
+  if (!aligned(q, 16) || !aligned(k, 16) || !aligned(b_rows, 4) || !aligned(m_rows, 4) ||
+      !aligned(mu, 4) || !aligned(kmax, 4) || !aligned(bmax, 4))
+    return WSATTN_ERR_BAD_ARG;
+  const int64_t bh64 = static_cast<int64_t>(batch) * heads;
+  // The scratch holds one chunk slot per (b, h) at the very least.
+  if (bh64 > kStaticSlots) return WSATTN_ERR_BAD_ARG;
+  if (bh64 * n_tokens >= (int64_t(1) << 31)) return WSATTN_ERR_BAD_ARG;
+  const int BH = static_cast<int>(bh64);
+  const int64_t N = n_tokens;
+
+  float* scratch = nullptr;
+  int num_sms = 0;
+  const int rc = scratch_for_current_device(&scratch, &num_sms);
+  if (rc != WSATTN_OK) return rc;
+
+  int nchunk = 0, rpc = 0;
+  prepare_chunking(BH, N, num_sms, &nchunk, &rpc);
+  if (static_cast<int64_t>(nchunk) * BH > kStaticSlots) {
+    // fewer, longer chunks so that every (b, h) fits in the slots
+    const int64_t max_chunks = kStaticSlots / BH;
+    int64_t r = (N + max_chunks - 1) / max_chunks;
+    r = (r + 15) / 16 * 16;
+    rpc = static_cast<int>(r);
+    nchunk = static_cast<int>((N + r - 1) / r);
+  }
+
+  PrepBuffers b;
+  b.b_rows = b_rows;
+  b.m_rows = m_rows;
+  b.mu = mu;
+  b.kmax = kmax;
+  b.bmax = bmax;
+  b.elig = elig;
+  b.part_sum = scratch;
+  b.part_kmax = scratch + static_cast<size_t>(kStaticSlots) * kStaticMaxDim;
+  b.part_qmax = b.part_kmax + kStaticSlots;
+  b.nchunk = nchunk;
+  b.rows_per_chunk = rpc;
+  const float scale = 1.0f / sqrtf(static_cast<float>(head_dim));
+  if (launch_prepare(q, k, BH, N, head_dim, scale, tau, b, static_cast<cudaStream_t>(stream)) !=
+      cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  return WSATTN_OK;
+}

@@ -129,6 +129,36 @@ int wsattn_prepare(wsattn_plan_t plan, int batch, const void* q, const void* k, 
 int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, const void* v,
                    float* out, void* stream);
 
+/*
+ * No-allocation variant of wsattn_prepare.  The paper has no counterpart: it
+ * exists for callers that must not let the library allocate device memory
+ * (a host framework that owns all device memory through its own pool or a
+ * fixed budget, or a latency-critical loop that cannot take cudaMalloc's
+ * implicit synchronisation).  It computes the same statistics as
+ * wsattn_prepare, with no plan, into buffers the caller owns, and never
+ * calls cudaMalloc, cudaFree or any other allocating routine.
+ *   batch, heads, n_tokens, head_dim   shape of q and k ([batch, heads,
+ *                     n_tokens, head_dim] bf16, 16-byte aligned); head_dim
+ *                     64 or 128
+ *   tau               eligibility threshold (> 0; the library default is 40)
+ *   b_rows, m_rows    fp32 [batch*heads*n_tokens] outputs: b_i and m_i
+ *   mu                fp32 [batch*heads*head_dim] output
+ *   kmax, bmax        fp32 [batch*heads] outputs: K_h and B_h
+ *   elig              uint8 [batch*heads] output
+ * Its scratch is one fixed array in the library's device image: 2048 chunk
+ * slots (1,064,960 bytes), held by every GPU that loads the library until
+ * the process exits.  batch*heads above 2048 is rejected with BAD_ARG before
+ * anything is enqueued.  All calls share the array and it keeps the last
+ * call's contents; nothing in it needs to start at zero.  Calls whose
+ * kernels can overlap on the GPU race on it and must be ordered by the
+ * caller.  The first call on a device looks up the array's device address
+ * with that device current (so make it before any stream capture).
+ * Errors: BAD_ARG, UNSUPPORTED (head_dim), CUDA.
+ */
+int wsattn_prepare_static(int batch, int heads, int n_tokens, int head_dim, float tau,
+                          const void* q, const void* k, float* b_rows, float* m_rows, float* mu,
+                          float* kmax, float* bmax, uint8_t* elig, void* stream);
+
 /* ---------------------------------------------------------- introspection */
 
 /* Plan geometry.  info[0..9] = N, block_q, block_k, q blocks, k blocks,

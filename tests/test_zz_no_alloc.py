@@ -1,0 +1,82 @@
+"""wsattn_prepare_static: the prepare statistics for callers that must not let
+the library allocate device memory (a framework that owns all device memory
+through its own pool or budget, or a latency-critical loop that cannot take
+cudaMalloc's implicit synchronisation).
+
+The entry point is called through the C ABI on two calls in a row, with
+different shapes, and each result is checked against the statistics the
+allocating entry point (wsattn_prepare) computes for the same input, within
+the tolerances the prepare parity tests use.  The output buffers are filled
+with NaN first, so every value checked was written by the call.  Free device
+memory is unchanged across the second call.
+"""
+import ctypes
+
+import numpy as np
+import pytest
+import torch
+
+from workloads import WORKLOADS, generate
+
+pytestmark = pytest.mark.gpu
+
+REL = 1e-5
+
+
+def _ptr(t):
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _reference_stats(wl, qd, kd):
+    import frame_aligned_window_gb300 as fw
+    plan = fw.wsattn_plan(wl.frames, wl.tokens_per_frame, wl.window, wl.ref_frames, wl.heads,
+                          wl.head_dim)
+    fw.wsattn_prepare(plan, qd, kd)
+    return fw.wsattn_get_stats(plan, wl.batch)
+
+
+def _call_static(wl, qd, kd, out):
+    import frame_aligned_window_gb300 as fw
+    fn = fw.raw_call("wsattn_prepare_static")
+    stream = ctypes.c_void_p(torch.cuda.current_stream().cuda_stream)
+    return fn(wl.batch, wl.heads, wl.n_tokens, wl.head_dim, ctypes.c_float(40.0), _ptr(qd),
+              _ptr(kd), _ptr(out["b"]), _ptr(out["m"]), _ptr(out["mu"]), _ptr(out["kmax"]),
+              _ptr(out["bmax"]), _ptr(out["elig"]), stream)
+
+
+def _check_against(out, ref):
+    got = {key: t.cpu().numpy() for key, t in out.items()}
+    np.testing.assert_array_equal(got["elig"], ref["elig"])
+    np.testing.assert_allclose(got["mu"], ref["mu"], rtol=0, atol=2e-5)
+    for key in ("b", "m", "kmax", "bmax"):
+        np.testing.assert_allclose(got[key], ref[key], rtol=REL, atol=1e-6)
+
+
+def test_prepare_static_two_calls_match_prepare():
+    import frame_aligned_window_gb300 as fw
+    for call, name in enumerate(["small", "tiny"]):
+        wl = WORKLOADS[name]
+        q, k, v = generate(wl)
+        qd, kd = q.cuda(), k.cuda()
+        ref = _reference_stats(wl, qd, kd)
+        out = fw.wsattn_prepare_static_outputs(wl.batch, wl.heads, wl.n_tokens, wl.head_dim)
+        for key, t in out.items():
+            t.fill_(255 if t.dtype == torch.uint8 else float("nan"))
+        torch.cuda.synchronize()
+        free_before = torch.cuda.mem_get_info()[0]
+        assert _call_static(wl, qd, kd, out) == 0
+        torch.cuda.synchronize()
+        if call == 1:
+            assert torch.cuda.mem_get_info()[0] == free_before
+        _check_against(out, ref)
+        assert torch.equal(kd.cpu(), k) and torch.equal(qd.cpu(), q)
+
+
+def test_prepare_static_rejects_sizes_beyond_its_scratch():
+    import frame_aligned_window_gb300 as fw
+    fn = fw.raw_call("wsattn_prepare_static")
+    t = torch.zeros(16, dtype=torch.float32, device="cuda")
+    p = _ptr(t)
+    # 2049 (b, h) pairs exceed the 2048 chunk slots: rejected before any launch
+    assert fn(1, 2049, 16, 64, ctypes.c_float(40.0), p, p, p, p, p, p, p, p, None) == 1
+    assert fn(1, 2, 16, 96, ctypes.c_float(40.0), p, p, p, p, p, p, p, p, None) == 3
