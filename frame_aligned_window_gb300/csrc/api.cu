@@ -22,7 +22,7 @@ struct wsattn_plan_s {
   size_t smem_optin = 0;
   int clock_khz = 0;
   WorkTile* d_tiles = nullptr;
-  int32_t* d_kcol = nullptr;
+  int32_t* d_cls = nullptr;
   int* d_status = nullptr;
   // statistics workspace, sized for ws_batch
   int ws_batch = 0;
@@ -77,14 +77,14 @@ int ensure_device(wsattn_plan_s* p) {
     return WSATTN_ERR_CUDA;
   const HostPlan& hp = p->hp;
   const size_t tiles_bytes = hp.tiles.size() * sizeof(WorkTile);
-  const size_t kcol_bytes = hp.kcol.size() * sizeof(int32_t);
+  const size_t cls_bytes = hp.cls.size() * sizeof(int32_t);
   if (cudaMalloc(&p->d_tiles, tiles_bytes) != cudaSuccess ||
-      cudaMalloc(&p->d_kcol, kcol_bytes) != cudaSuccess ||
+      cudaMalloc(&p->d_cls, cls_bytes) != cudaSuccess ||
       cudaMalloc(&p->d_status, sizeof(int)) != cudaSuccess)
     return WSATTN_ERR_CUDA;
   if (cudaMemcpy(p->d_tiles, hp.tiles.data(), tiles_bytes, cudaMemcpyHostToDevice) !=
           cudaSuccess ||
-      cudaMemcpy(p->d_kcol, hp.kcol.data(), kcol_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemcpy(p->d_cls, hp.cls.data(), cls_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
       cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess)
     return WSATTN_ERR_CUDA;
   p->device = dev;
@@ -144,11 +144,11 @@ int ensure_workspace(wsattn_plan_s* p, int batch, cudaStream_t stream) {
 
 void free_device(wsattn_plan_s* p) {
   if (p->d_tiles) cudaFree(p->d_tiles);
-  if (p->d_kcol) cudaFree(p->d_kcol);
+  if (p->d_cls) cudaFree(p->d_cls);
   if (p->d_status) cudaFree(p->d_status);
   if (p->ws) cudaFree(p->ws);
   p->d_tiles = nullptr;
-  p->d_kcol = nullptr;
+  p->d_cls = nullptr;
   p->d_status = nullptr;
   p->ws = nullptr;
 }
@@ -222,7 +222,8 @@ int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, 
       !encode_map(&prm.tm_k, k, rows, hp.D, hp.bk) || !encode_map(&prm.tm_v, v, rows, hp.D, hp.bk))
     return WSATTN_ERR_CUDA;
   prm.tiles = plan->d_tiles;
-  prm.kcol = plan->d_kcol;
+  prm.cls = plan->d_cls;
+  prm.n_cls = static_cast<int>(hp.cls.size()) - 1;
   prm.m_rows = plan->buf.m_rows;
   prm.elig = plan->buf.elig;
   prm.out = out;
@@ -231,10 +232,14 @@ int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, 
   prm.bh = BH;
   prm.n = static_cast<int>(hp.N);
   prm.bk = hp.bk;
-  wsattn::forward_stages(hp.D, hp.bk, plan->smem_optin, &prm.stages_k, &prm.stages_v);
+  prm.G = hp.G;
+  // K and V boxes are one key block; a step of G blocks issues G boxes into
+  // consecutive rows of its stage.
+  const int step_keys = hp.G * hp.bk;
+  wsattn::forward_stages(hp.D, step_keys, plan->smem_optin, &prm.stages_k, &prm.stages_v);
   prm.force_path = plan->force_path;
   prm.scale_log2 = (1.0f / std::sqrt(static_cast<float>(hp.D))) * 1.4426950408889634f;
-  const size_t smem = wsattn::forward_smem_bytes(hp.D, hp.bk, prm.stages_k, prm.stages_v);
+  const size_t smem = wsattn::forward_smem_bytes(hp.D, step_keys, prm.stages_k, prm.stages_v);
   if (prm.stages_k < 2 || smem > plan->smem_optin) return WSATTN_ERR_UNSUPPORTED;
   const int64_t items = static_cast<int64_t>(prm.n_tiles) * BH;
   const int grid = static_cast<int>(items < plan->num_sms ? items : plan->num_sms);

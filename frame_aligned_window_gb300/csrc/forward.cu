@@ -9,23 +9,41 @@
 //     row bound is the softmax max, so a block's probabilities are
 //     p = exp(scale*s - m_i) with no running max and no rescale in the loop
 //     (m_i = b_i + scale q_i.mu: the bound of the centered logits, shifted
-//     back to the logits of the keys as given);
-//     ineligible heads run the online max (rescaling O and l) in the same
-//     kernel, chosen per tile.
+//     back to the logits of the keys as given); ineligible heads run the
+//     online max (rescaling O and l) in the same kernel, chosen per tile.
 //   - "Proving pixels unchanged": the PV product takes P in bf16.
 //
-// Persistent kernel, one CTA per SM, 8 warps:
+// Persistent kernel, one CTA per SM, 12 warps:
 //   warp 0      TMA producer: Q tile (128 x D) into a staging buffer; K and V
-//               blocks (bk x D) into two rings, all 128-byte swizzled.
+//               steps into two rings, all 128-byte swizzled.
 //   warp 1      MMA issuer (one thread): S = Q K^T and O += P V with
 //               tcgen05.mma kind::f16 (bf16 in, fp32 accumulate in TMEM).
 //               Q and P are read from TMEM, K and V from shared memory.
-//   warps 4-7   softmax + epilogue warpgroup: thread i owns row i of the
-//               tile (TMEM lane i), so row sums are thread-local.
-// Tensor memory (512 columns): O [0, D), S0/S1 double buffer of bk columns
-// each (P aliases the first bk/2 columns of its S buffer as bf16 pairs), Q
-// (D/2 columns of bf16 pairs).  While the softmax works on S(j), the tensor
-// core runs PV(j-1) and QK(j+1).
+//   warp 2      allocates and frees tensor memory.
+//   warps 4-11  two softmax + epilogue warpgroups.  Thread i of a warpgroup
+//               owns row i of the tile (TMEM lane i); warpgroup 0 takes the
+//               first s columns of every key step, warpgroup 1 the rest
+//               (s = 16 * ceil(keys / 32)), so each SMSP runs two softmax warps.
+//
+// Keys are consumed in steps of up to G consecutive active blocks of one run
+// (G * bk <= 160 keys): one TMA box per block lands in consecutive rows of the
+// step's stage (the swizzle pattern continues across boxes), and each MMA
+// covers the whole step, so the per-step handoffs (barrier waits, commits,
+// softmax rounds) are amortised over up to 160 keys.
+//
+// Tensor memory (512 columns): O [0, D), S0/S1 double buffer of G*bk columns
+// each, Q (D/2 columns of bf16 pairs).  P (keys/2 columns of bf16 pairs)
+// aliases its S buffer from column s/2: warpgroup 0's half lands in columns
+// [s/2, s) and warpgroup 1's in [s, s/2 + keys/2).  Warpgroup 0 walks its
+// 16-column chunks backwards and warpgroup 1 forwards, so every chunk's P
+// lands in S columns its own warpgroup has already read: the two never wait
+// on each other in the fixed-max path, and each holds one chunk (plus the
+// next one in flight) in registers.  While the softmax works on S(j), the
+// tensor core runs PV(j-1) and QK(j+1).
+//
+// Work items (tile, b*h) go class by class (tiles with equal key lists,
+// longest first) and head by head inside a class, so the CTAs running at one
+// time stream the same head's keys and values through L2.
 //
 // Every wait is bounded: on expiry the kernel sets a bit in the status word,
 // raises a CTA-wide abort flag, and all roles leave their loops; TMEM is
@@ -40,8 +58,10 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 256;
+constexpr int kThreads = 384;
 constexpr int kSoftmaxWarp0 = 4;
+constexpr int kSoftmaxThreads = 256;
+constexpr int kMaxChunksAll = 5;  // 16-column chunks a warpgroup takes at 160 keys
 constexpr long long kWaitLimitCycles = 1LL << 31;  // about one second
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;
@@ -57,15 +77,21 @@ enum : int {
   B_SFULL1,
   B_PFULL0,      // softmax -> MMA: P buffer 0 / 1 written
   B_PFULL1,
+  B_XCH,         // softmax <-> softmax: row maxima / row sums exchanged
   B_KFULL0,
   B_KEMPTY0 = B_KFULL0 + 4,
   B_VFULL0 = B_KEMPTY0 + 4,
   B_VEMPTY0 = B_VFULL0 + 4,
   B_COUNT = B_VEMPTY0 + 4
 };
+// Exchange area after the barriers: row maxima and row sums of the two
+// warpgroups, double-buffered: float [2 parity][2 warpgroups][128 rows] each.
+constexpr uint32_t kXchBytes = 2 * 2 * 2 * 128 * 4;
 
 struct Shared {
   uint32_t q, k, v, bars;  // shared-window addresses
+  float* xch_m;            // [2][2][128]
+  float* xch_l;            // [2][2][128]
   volatile int* abort_flag;
   int* status;
 };
@@ -99,161 +125,254 @@ __device__ __forceinline__ bool wait_warp(const Shared& s, uint32_t b, uint32_t 
   return __all_sync(0xffffffffu, ok);
 }
 
+// Barrier of the two softmax warpgroups (all 256 threads arrive, then wait
+// for the phase), bounded like every other wait; the arrive publishes the
+// exchange values written before it.
+__device__ __forceinline__ bool xch_sync(const Shared& s, uint32_t& xc) {
+  mbar_arrive(bar(s, B_XCH));
+  const bool ok = wait_warp(s, bar(s, B_XCH), xc & 1u);
+  ++xc;
+  return ok;
+}
+
+// First S column of warpgroup 1 in a step of `keys` keys; P starts at s/2.
+__device__ __forceinline__ int split_col(int keys) { return 16 * ((keys / 16 + 1) / 2); }
+
 struct TmemCols {
   uint32_t o, s0, s1, q;
 };
 
 template <int D>
-__device__ __forceinline__ TmemCols tmem_cols(int bk) {
-  const uint32_t spad = (static_cast<uint32_t>(bk) + 31u) & ~31u;
+__device__ __forceinline__ TmemCols tmem_cols(int step_keys) {
+  const uint32_t spad = (static_cast<uint32_t>(step_keys) + 31u) & ~31u;
   return TmemCols{0u, static_cast<uint32_t>(D), static_cast<uint32_t>(D) + spad,
                   static_cast<uint32_t>(D) + 2u * spad};
 }
+
+struct Item {
+  int tile, bh;
+};
+
+// Work item -> (tile, b*h): classes in order, heads in order inside a class.
+__device__ __forceinline__ Item map_item(const FwdParams& p, int it) {
+  int c = 0;
+  while (c + 1 < p.n_cls && it >= p.bh * __ldg(p.cls + c + 1)) ++c;
+  const int beg = __ldg(p.cls + c);
+  const int n = __ldg(p.cls + c + 1) - beg;
+  const int o = it - p.bh * beg;
+  return Item{beg + o % n, o / n};
+}
+
+// Position in a ring of `n` stages: slot and the parity of its current use.
+// Advanced by increments only (no division in the per-step loops).
+struct Ring {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ void next(uint32_t n) {
+    if (++slot == n) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
+// Walks a tile's key steps: up to G consecutive blocks of the first run, then
+// of the second.
+struct Steps {
+  int kb, left, run1, len1;
+  __device__ __forceinline__ void init(const WorkTile& t) {
+    kb = t.run0;
+    left = t.len0;
+    run1 = t.run1;
+    len1 = t.nblk - t.len0;
+  }
+  // First block of the next step; nb receives its block count.
+  __device__ __forceinline__ int next(int G, int& nb) {
+    if (left == 0) {
+      kb = run1;
+      left = len1;
+      len1 = 0;
+    }
+    nb = left < G ? left : G;
+    const int first = kb;
+    kb += nb;
+    left -= nb;
+    return first;
+  }
+};
 
 // ------------------------------------------------------------------ producer
 template <int D>
 __device__ void producer(const FwdParams& p, const Shared& s) {
   constexpr int kBoxes = D / 64;
-  const uint32_t box_bytes = static_cast<uint32_t>(p.bk) * 128u;
-  const uint32_t stage_bytes = box_bytes * kBoxes;
+  const int bk = p.bk, G = p.G;
+  const uint32_t ns = static_cast<uint32_t>(G * bk);     // rows of a full step
+  const uint32_t box_pitch = ns * 128u;                  // a 64-column box of a stage
+  const uint32_t stage_bytes = box_pitch * kBoxes;
+  const uint32_t blk_rows_bytes = static_cast<uint32_t>(bk) * 128u;
+  const uint32_t blk_tx = static_cast<uint32_t>(bk) * D * 2u;
   const int n_items = p.n_tiles * p.bh;
-  uint32_t kc = 0, vc = 0, qc = 0;
+  const uint32_t nk = static_cast<uint32_t>(p.stages_k), nv = static_cast<uint32_t>(p.stages_v);
+  Ring kr, vr;
+  uint32_t qc = 0;
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const WorkTile t = p.tiles[it / p.bh];
-    const int y0 = (it % p.bh) * p.n;
+    const Item im = map_item(p, it);
+    const WorkTile t = p.tiles[im.tile];
+    const int y0 = im.bh * p.n;
     if (!wait(s, bar(s, B_QEMPTY), (qc & 1u) ^ 1u, kStatusTimeoutProducer)) return;
     mbar_arrive_expect_tx(bar(s, B_QFULL), kTileM * D * 2);
 #pragma unroll
     for (int c = 0; c < kBoxes; ++c)
       tma_load_2d(s.q + c * (kTileM * 128), &p.tm_q, bar(s, B_QFULL), c * 64, y0 + t.row0);
     ++qc;
-    const int nblk = t.kend - t.kbeg;
+    Steps ks, vs;
+    ks.init(t);
+    vs.init(t);
     // Issue order follows consumption: K0, K1, V0, K2, V1, ...
-    for (int j = 0; j <= nblk; ++j) {
-      if (j < nblk) {
-        const int row = y0 + p.kcol[t.kbeg + j] * p.bk;
-        const uint32_t slot = kc % static_cast<uint32_t>(p.stages_k);
-        const uint32_t ph = (kc / static_cast<uint32_t>(p.stages_k)) & 1u;
-        if (!wait(s, bar(s, B_KEMPTY0 + slot), ph ^ 1u, kStatusTimeoutProducer)) return;
-        mbar_arrive_expect_tx(bar(s, B_KFULL0 + slot), stage_bytes);
+    for (int j = 0; j <= t.nstep; ++j) {
+      if (j < t.nstep) {
+        int nb;
+        const int first = ks.next(G, nb);
+        if (!wait(s, bar(s, B_KEMPTY0 + kr.slot), kr.phase ^ 1u, kStatusTimeoutProducer)) return;
+        const uint32_t fb = bar(s, B_KFULL0 + kr.slot);
+        mbar_arrive_expect_tx(fb, blk_tx * nb);
+        const uint32_t dst = s.k + kr.slot * stage_bytes;
+        for (int b = 0; b < nb; ++b) {
+          const int row = y0 + (first + b) * bk;
 #pragma unroll
-        for (int c = 0; c < kBoxes; ++c)
-          tma_load_2d(s.k + slot * stage_bytes + c * box_bytes, &p.tm_k, bar(s, B_KFULL0 + slot),
-                      c * 64, row);
-        ++kc;
+          for (int c = 0; c < kBoxes; ++c)
+            tma_load_2d(dst + c * box_pitch + b * blk_rows_bytes, &p.tm_k, fb, c * 64, row);
+        }
+        kr.next(nk);
       }
       if (j >= 1) {
-        const int row = y0 + p.kcol[t.kbeg + j - 1] * p.bk;
-        const uint32_t slot = vc % static_cast<uint32_t>(p.stages_v);
-        const uint32_t ph = (vc / static_cast<uint32_t>(p.stages_v)) & 1u;
-        if (!wait(s, bar(s, B_VEMPTY0 + slot), ph ^ 1u, kStatusTimeoutProducer)) return;
-        mbar_arrive_expect_tx(bar(s, B_VFULL0 + slot), stage_bytes);
+        int nb;
+        const int first = vs.next(G, nb);
+        if (!wait(s, bar(s, B_VEMPTY0 + vr.slot), vr.phase ^ 1u, kStatusTimeoutProducer)) return;
+        const uint32_t fb = bar(s, B_VFULL0 + vr.slot);
+        mbar_arrive_expect_tx(fb, blk_tx * nb);
+        const uint32_t dst = s.v + vr.slot * stage_bytes;
+        for (int b = 0; b < nb; ++b) {
+          const int row = y0 + (first + b) * bk;
 #pragma unroll
-        for (int c = 0; c < kBoxes; ++c)
-          tma_load_2d(s.v + slot * stage_bytes + c * box_bytes, &p.tm_v, bar(s, B_VFULL0 + slot),
-                      c * 64, row);
-        ++vc;
+          for (int c = 0; c < kBoxes; ++c)
+            tma_load_2d(dst + c * box_pitch + b * blk_rows_bytes, &p.tm_v, fb, c * 64, row);
+        }
+        vr.next(nv);
       }
     }
   }
 }
 
 // ---------------------------------------------------------------- MMA issuer
-template <int D>
+// One thread.  Descriptor bases are computed once; each MMA adds a constant
+// to the start-address field (bits 0-13, address >> 4), and both k-step loops
+// are unrolled, so the thread spends a few instructions per MMA.
+template <int D, int MAXC>
 __device__ void mma_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
   constexpr int kBoxes = D / 64;
-  const int bk = p.bk;
-  const uint32_t box_bytes = static_cast<uint32_t>(bk) * 128u;
-  const uint32_t stage_bytes = box_bytes * kBoxes;
-  const TmemCols tc_ = tmem_cols<D>(bk);
+  const int bk = p.bk, G = p.G;
+  const int ns = G * bk;
+  const uint32_t box_pitch = static_cast<uint32_t>(ns) * 128u;
+  const uint32_t stage_bytes = box_pitch * kBoxes;
+  const TmemCols tc_ = tmem_cols<D>(ns);
   const uint32_t t_o = tbase + tc_.o, t_s0 = tbase + tc_.s0, t_s1 = tbase + tc_.s1;
   const uint32_t t_q = tbase + tc_.q;
-  const uint32_t id_qk = idesc_bf16_f32(kTileM, bk, false);
+  const uint32_t id_qk0 = idesc_bf16_f32(kTileM, 0, false);  // N filled per step
   const uint32_t id_pv = idesc_bf16_f32(kTileM, D, true);
+  // K is K-major (SBO 1 KB); V is MN-major (LBO = the 64-column box pitch).
+  const uint64_t kdesc0 = sdesc_sw128(s.k, 16, 1024);
+  const uint64_t vdesc0 = sdesc_sw128(s.v, box_pitch, 1024);
+  const uint64_t box16 = box_pitch >> 4, stage16 = stage_bytes >> 4;
   const int n_items = p.n_tiles * p.bh;
-  uint32_t kc = 0, vc = 0, pc0 = 0, pc1 = 0, tiles_done = 0;
+  const uint32_t nk = static_cast<uint32_t>(p.stages_k), nv = static_cast<uint32_t>(p.stages_v);
+  Ring kr, vr;
+  uint32_t pc0 = 0, pc1 = 0, tiles_done = 0;
+  Steps qs, ps;
 
   // S(j) = Q K_j^T into S buffer (j & 1).
   auto issue_qk = [&](int j) -> bool {
-    const uint32_t slot = kc % static_cast<uint32_t>(p.stages_k);
-    const uint32_t ph = (kc / static_cast<uint32_t>(p.stages_k)) & 1u;
-    if (!wait(s, bar(s, B_KFULL0 + slot), ph, kStatusTimeoutMma)) return false;
+    int nb;
+    qs.next(G, nb);
+    const uint32_t keys = static_cast<uint32_t>(nb * bk);
+    const uint32_t slot = kr.slot;
+    if (!wait(s, bar(s, B_KFULL0 + slot), kr.phase, kStatusTimeoutMma)) return false;
     tc_fence_after();
-    const uint32_t kbase = s.k + slot * stage_bytes;
+    const uint64_t kd = kdesc0 + slot * stage16;
     const uint32_t d_s = (j & 1) ? t_s1 : t_s0;
+    const uint32_t id = id_qk0 | ((keys >> 3) << 17);
 #pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk) {
-      const uint64_t bdesc = sdesc_sw128(kbase + (kk / 4) * box_bytes + (kk % 4) * 32, 16, 1024);
-      mma_ts(d_s, t_q + kk * 8, bdesc, id_qk, kk > 0 ? 1u : 0u);
-    }
+    for (int kk = 0; kk < D / 16; ++kk)
+      mma_ts(d_s, t_q + kk * 8, kd + (kk / 4) * box16 + (kk % 4) * 2, id, kk > 0 ? 1u : 0u);
     tc_commit(bar(s, B_KEMPTY0 + slot));
     tc_commit(bar(s, (j & 1) ? B_SFULL1 : B_SFULL0));
-    ++kc;
+    kr.next(nk);
     return true;
   };
 
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
-    const WorkTile t = p.tiles[it / p.bh];
-    const int bh = it % p.bh;
-    const int nblk = t.kend - t.kbeg;
-    const bool online = p.force_path >= 0 ? (p.force_path == 1) : (p.elig[bh] == 0);
+    const Item im = map_item(p, it);
+    const WorkTile t = p.tiles[im.tile];
+    const int nstep = t.nstep;
+    const bool online = p.force_path >= 0 ? (p.force_path == 1) : (p.elig[im.bh] == 0);
+    qs.init(t);
+    ps.init(t);
     if (!wait(s, bar(s, B_QTFULL), tiles_done & 1u, kStatusTimeoutMma)) return;
     tc_fence_after();
-    for (int j = 0; j < nblk && j < 2; ++j)
+    for (int j = 0; j < nstep && j < 2; ++j)
       if (!issue_qk(j)) return;
-    for (int j = 0; j < nblk; ++j) {
+    for (int j = 0; j < nstep; ++j) {
+      int nb;
+      ps.next(G, nb);
+      const int keys = nb * bk;
+      const int nks = keys / 16;
       const int sb = j & 1;
       uint32_t par;
       if (sb) { par = pc1 & 1u; ++pc1; } else { par = pc0 & 1u; ++pc0; }
       if (!wait(s, bar(s, B_PFULL0 + sb), par, kStatusTimeoutMma)) return;
+      const uint32_t vslot = vr.slot;
+      if (!wait(s, bar(s, B_VFULL0 + vslot), vr.phase, kStatusTimeoutMma)) return;
       tc_fence_after();
-      const uint32_t vslot = vc % static_cast<uint32_t>(p.stages_v);
-      const uint32_t vph = (vc / static_cast<uint32_t>(p.stages_v)) & 1u;
-      if (!wait(s, bar(s, B_VFULL0 + vslot), vph, kStatusTimeoutMma)) return;
-      tc_fence_after();
-      const uint32_t vbase = s.v + vslot * stage_bytes;
-      const uint32_t a_p = sb ? t_s1 : t_s0;
-      for (int kk = 0; kk < bk / 16; ++kk) {
-        // V is MN-major: 16 key rows per step (2 KB), D split in 64-wide
-        // boxes box_bytes apart (leading byte offset), 8-row groups 1 KB apart.
-        const uint64_t bdesc = sdesc_sw128(vbase + kk * 2048, box_bytes, 1024);
-        mma_ts(t_o, a_p + kk * 8, bdesc, id_pv, (j > 0 || kk > 0) ? 1u : 0u);
-      }
+      const uint64_t vd = vdesc0 + vslot * stage16;
+      const uint32_t a_p = (sb ? t_s1 : t_s0) + static_cast<uint32_t>(split_col(keys) / 2);
+      // 16 key rows (2 KB of V) per k-step
+      mma_ts(t_o, a_p, vd, id_pv, j > 0 ? 1u : 0u);
+#pragma unroll
+      for (int kk = 1; kk < 2 * MAXC; ++kk)
+        if (kk < nks) mma_ts(t_o, a_p + kk * 8, vd + kk * 128, id_pv, 1u);
       tc_commit(bar(s, B_VEMPTY0 + vslot));
-      ++vc;
-      if (online && j + 1 < nblk) tc_commit(bar(s, B_OBAR));
-      if (j + 2 < nblk && !issue_qk(j + 2)) return;
+      vr.next(nv);
+      if (online && j + 1 < nstep) tc_commit(bar(s, B_OBAR));
+      if (j + 2 < nstep && !issue_qk(j + 2)) return;
     }
     tc_commit(bar(s, B_OFULL));
     ++tiles_done;
   }
 }
 
-// -------------------------------------------------------------- softmax WG
-// Copies this thread's Q row from the swizzled staging tile into TMEM (bf16
-// pairs, column c holds elements 2c, 2c+1); rows past the frame are zeroed.
+// -------------------------------------------------------------- softmax WGs
+// Copies this thread's share of its Q row (elements [wg D/2, (wg+1) D/2))
+// from the swizzled staging tile into TMEM (column c holds elements 2c and
+// 2c+1); rows past the frame are zeroed.
 template <int D>
-__device__ bool load_q(const Shared& s, uint32_t t_q, int r, int nvalid, uint32_t& qc) {
+__device__ bool load_q(const Shared& s, uint32_t t_q, int wg, int r, int nvalid, uint32_t& qc) {
   if (!wait_warp(s, bar(s, B_QFULL), qc & 1u)) return false;
   ++qc;
   const bool zero = r >= nvalid;
 #pragma unroll
-  for (int c = 0; c < D / 64; ++c) {
-    const uint32_t row_addr = s.q + c * (kTileM * 128) + r * 128;
+  for (int h = 0; h < D / 32; ++h) {
+    const int e0 = wg * (D / 2) + 16 * h;  // first element of this 16-element group
+    const uint32_t row_addr = s.q + (e0 / 64) * (kTileM * 128) + r * 128;
+    uint32_t w[8];
 #pragma unroll
-    for (int h = 0; h < 4; ++h) {
-      uint32_t w[8];
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const uint32_t m = static_cast<uint32_t>(2 * h + e);
-        const uint4 v = ld_shared_v4(row_addr + ((m ^ static_cast<uint32_t>(r & 7)) << 4));
-        w[4 * e + 0] = zero ? 0u : v.x;
-        w[4 * e + 1] = zero ? 0u : v.y;
-        w[4 * e + 2] = zero ? 0u : v.z;
-        w[4 * e + 3] = zero ? 0u : v.w;
-      }
-      tmem_st8(t_q + c * 32 + h * 8, w);
+    for (int e = 0; e < 2; ++e) {
+      const uint32_t m = static_cast<uint32_t>((e0 % 64) / 8 + e);
+      const uint4 v = ld_shared_v4(row_addr + ((m ^ static_cast<uint32_t>(r & 7)) << 4));
+      w[4 * e + 0] = zero ? 0u : v.x;
+      w[4 * e + 1] = zero ? 0u : v.y;
+      w[4 * e + 2] = zero ? 0u : v.z;
+      w[4 * e + 3] = zero ? 0u : v.w;
     }
+    tmem_st8(t_q + e0 / 2, w);
   }
   tmem_wait_st();
   tc_fence_before();
@@ -262,109 +381,124 @@ __device__ bool load_q(const Shared& s, uint32_t t_q, int r, int nvalid, uint32_
   return true;
 }
 
-// p = 2^(s*c + nb) for 16 logits; adds them to l (pairwise) and stores the
-// bf16 pairs as 8 TMEM columns at taddr.
-__device__ __forceinline__ void exp_pack_store(const uint32_t (&sv)[16], float c, float nb,
-                                               float& l, uint32_t taddr) {
+// p = 2^(s*c + nb) for 16 logits (two lanes at a time); adds them to the
+// packed row sums and stores the bf16 pairs as 8 TMEM columns at taddr.
+__device__ __forceinline__ void exp_pack_store(const uint32_t (&sv)[16], uint64_t c2, uint64_t nb2,
+                                               uint64_t& la, uint64_t& lb, uint32_t taddr) {
   uint32_t w[8];
-  float ps[8];
 #pragma unroll
   for (int i = 0; i < 8; ++i) {
-    const float p0 = ex2_approx(fmaf(__uint_as_float(sv[2 * i]), c, nb));
-    const float p1 = ex2_approx(fmaf(__uint_as_float(sv[2 * i + 1]), c, nb));
-    ps[i] = p0 + p1;
+    const float2 t = f2_unpack(
+        f2_fma(f2_pack(__uint_as_float(sv[2 * i]), __uint_as_float(sv[2 * i + 1])), c2, nb2));
+    const float p0 = ex2_approx(t.x);
+    const float p1 = ex2_approx(t.y);
+    if (i & 1)
+      lb = f2_add(lb, f2_pack(p0, p1));
+    else
+      la = f2_add(la, f2_pack(p0, p1));
     const __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);
     w[i] = *reinterpret_cast<const uint32_t*>(&h);
   }
   tmem_st8(taddr, w);
-  l += ((ps[0] + ps[1]) + (ps[2] + ps[3])) + ((ps[4] + ps[5]) + (ps[6] + ps[7]));
 }
 
-// Fixed-max path: nb = -m_i * log2(e).
-__device__ __forceinline__ bool fixed_block(uint32_t sa, int nch, float c, float nb, float& l0,
-                                            float& l1) {
+// Turns this warpgroup's n16 (<= MAXC) chunks of 16 S columns into P, one
+// chunk at a time with the next chunk's TMEM load in flight.  Chunk k sits at
+// S columns sa + 16k and its P at pa + 8k.  Warpgroup 0 (pa = sa + 8 n16)
+// walks its chunks backwards and warpgroup 1 (pa = sa) forwards: either way
+// a chunk's P lands only in S columns already read, so nothing is clobbered
+// before it is loaded.
+template <int MAXC>
+__device__ __forceinline__ void step_exp(uint32_t sa, uint32_t pa, int n16, bool reverse,
+                                         uint64_t c2, uint64_t nb2, uint64_t& la, uint64_t& lb) {
   uint32_t ra[16], rb[16];
-  tmem_ld16(sa, ra);
-  tmem_wait_ld16(ra);
-  for (int k = 0; k < nch; k += 2) {
-    const bool has_b = k + 1 < nch;
-    if (has_b) tmem_ld16(sa + (k + 1) * 16, rb);
-    exp_pack_store(ra, c, nb, l0, sa + k * 8);
-    if (has_b) {
-      tmem_wait_ld16(rb);
-      const bool has_a = k + 2 < nch;
-      if (has_a) tmem_ld16(sa + (k + 2) * 16, ra);
-      exp_pack_store(rb, c, nb, l1, sa + (k + 1) * 8);
-      if (has_a) tmem_wait_ld16(ra);
+  auto chunk = [&](int i) { return reverse ? n16 - 1 - i : i; };
+  if (n16 > 0) {
+    tmem_ld16(sa + 16 * chunk(0), ra);
+    tmem_wait_ld16(ra);
+  }
+#pragma unroll
+  for (int i = 0; i < MAXC; i += 2) {
+    if (i < n16) {
+      if (i + 1 < n16) tmem_ld16(sa + 16 * chunk(i + 1), rb);
+      exp_pack_store(ra, c2, nb2, la, lb, pa + 8 * chunk(i));
+      if (i + 1 < n16) tmem_wait_ld16(rb);
+    }
+    if (i + 1 < n16) {
+      if (i + 2 < n16) tmem_ld16(sa + 16 * chunk(i + 2), ra);
+      exp_pack_store(rb, c2, nb2, la, lb, pa + 8 * chunk(i + 1));
+      if (i + 2 < n16) tmem_wait_ld16(ra);
     }
   }
-  return true;
 }
 
-template <int D>
+template <int D, int MAXC>
 __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) {
   const int warp = threadIdx.x / 32;
-  const int r = threadIdx.x - kSoftmaxWarp0 * 32;  // tile row == TMEM lane
+  const int wg = (warp - kSoftmaxWarp0) / 4;
+  const int r = (threadIdx.x - kSoftmaxWarp0 * 32) % kTileM;  // tile row == TMEM lane
   const uint32_t lane = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
-  const TmemCols tc_ = tmem_cols<D>(p.bk);
-  const int nch = p.bk / 16;
+  const int bk = p.bk, G = p.G;
+  const TmemCols tc_ = tmem_cols<D>(G * bk);
+  const uint32_t ocol = tc_.o + static_cast<uint32_t>(wg * (D / 2));  // this WG's O half
   const float c = p.scale_log2;
+  const uint64_t c2 = f2_pack(c, c);
   const int n_items = p.n_tiles * p.bh;
-  uint32_t qc = 0, sc0 = 0, sc1 = 0, oc = 0, tiles_done = 0;
+  uint32_t qc = 0, sc0 = 0, sc1 = 0, oc = 0, tiles_done = 0, xpar = 0, xc = 0;
 
   int it = blockIdx.x;
   if (it >= n_items) return;
-  if (!load_q<D>(s, lane + tc_.q, r, p.tiles[it / p.bh].nvalid, qc)) return;
+  if (!load_q<D>(s, lane + tc_.q, wg, r, p.tiles[map_item(p, it).tile].nvalid, qc)) return;
   while (true) {
-    const WorkTile t = p.tiles[it / p.bh];
-    const int bh = it % p.bh;
-    const int nblk = t.kend - t.kbeg;
-    const bool online = p.force_path >= 0 ? (p.force_path == 1) : (p.elig[bh] == 0);
+    const Item im = map_item(p, it);
+    const WorkTile t = p.tiles[im.tile];
+    const bool online = p.force_path >= 0 ? (p.force_path == 1) : (p.elig[im.bh] == 0);
     const bool valid = r < t.nvalid;
-    const size_t grow = static_cast<size_t>(bh) * p.n + t.row0 + r;
+    const size_t grow = static_cast<size_t>(im.bh) * p.n + t.row0 + r;
+    Steps st;
+    st.init(t);
     float l = 0.f;
-    if (!online) {
-      const float nb = valid ? -p.m_rows[grow] * kLog2e : 0.f;
-      float l0 = 0.f, l1 = 0.f;
-      for (int j = 0; j < nblk; ++j) {
-        const int sb = j & 1;
-        uint32_t par;
-        if (sb) { par = sc1 & 1u; ++sc1; } else { par = sc0 & 1u; ++sc0; }
-        if (!wait_warp(s, bar(s, B_SFULL0 + sb), par)) return;
-        tc_fence_after();
-        fixed_block(lane + (sb ? tc_.s1 : tc_.s0), nch, c, nb, l0, l1);
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(s, B_PFULL0 + sb));
-      }
-      l = l0 + l1;
-    } else {
-      float m = -INFINITY;
-      for (int j = 0; j < nblk; ++j) {
-        const int sb = j & 1;
-        uint32_t par;
-        if (sb) { par = sc1 & 1u; ++sc1; } else { par = sc0 & 1u; ++sc0; }
-        if (!wait_warp(s, bar(s, B_SFULL0 + sb), par)) return;
-        tc_fence_after();
-        const uint32_t sa = lane + (sb ? tc_.s1 : tc_.s0);
+    float m = -INFINITY;
+    const float nb_fixed = valid ? -p.m_rows[grow] * kLog2e : 0.f;
+    uint64_t la = f2_pack(0.f, 0.f), lb = la;
+    for (int j = 0; j < t.nstep; ++j) {
+      int nblk;
+      st.next(G, nblk);
+      const int keys = nblk * bk;
+      const int split = split_col(keys);
+      const uint32_t c0 = wg == 0 ? 0u : static_cast<uint32_t>(split);  // first S column
+      const int n16 = (wg == 0 ? split : keys - split) / 16;           // 16-column chunks
+      const uint32_t pcol = static_cast<uint32_t>(split / 2) + c0 / 2;  // first P column
+      const int sb = j & 1;
+      uint32_t par;
+      if (sb) { par = sc1 & 1u; ++sc1; } else { par = sc0 & 1u; ++sc0; }
+      if (!wait_warp(s, bar(s, B_SFULL0 + sb), par)) return;
+      tc_fence_after();
+      const uint32_t sbase = lane + (sb ? tc_.s1 : tc_.s0);
+      if (!online) {
+        step_exp<MAXC>(sbase + c0, sbase + pcol, n16, wg == 0, c2, f2_pack(nb_fixed, nb_fixed), la,
+                       lb);
+      } else {
+        // row max of this step over both warpgroups' columns, one chunk at a time
         float mx = -INFINITY;
-        for (int k = 0; k < nch; ++k) {
+        for (int k = 0; k < n16; ++k) {
           uint32_t ra[16];
-          tmem_ld16(sa + k * 16, ra);
+          tmem_ld16(sbase + c0 + 16 * k, ra);
           tmem_wait_ld16(ra);
 #pragma unroll
           for (int i = 0; i < 16; ++i) mx = fmaxf(mx, __uint_as_float(ra[i]));
         }
-        const float m_new = fmaxf(m, mx * c);
+        s.xch_m[(xpar * 2 + wg) * kTileM + r] = mx;
+        if (!xch_sync(s, xc)) return;
+        const float mo = s.xch_m[(xpar * 2 + (wg ^ 1)) * kTileM + r];
+        xpar ^= 1u;
+        const float m_new = fmaxf(m, fmaxf(mx, mo) * c);
         const float alpha = ex2_approx(m - m_new);
-        float ls = 0.f;
-        for (int k = 0; k < nch; ++k) {
-          uint32_t ra[16];
-          tmem_ld16(sa + k * 16, ra);
-          tmem_wait_ld16(ra);
-          exp_pack_store(ra, c, -m_new, ls, sa + k * 8);
-        }
-        l = l * alpha + ls;
+        uint64_t sa2 = f2_pack(0.f, 0.f), sb2 = sa2;
+        step_exp<MAXC>(sbase + c0, sbase + pcol, n16, wg == 0, c2, f2_pack(-m_new, -m_new), sa2,
+                       sb2);
+        const float2 a = f2_unpack(f2_add(sa2, sb2));
+        l = l * alpha + (a.x + a.y);
         m = m_new;
         if (j > 0) {
           // O += P(j-1) V must have landed before it is rescaled.
@@ -372,35 +506,53 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
           ++oc;
           tc_fence_after();
           if (__any_sync(0xffffffffu, alpha < 1.f)) {
-            for (int k = 0; k < D / 16; ++k) {
+            const uint64_t a2 = f2_pack(alpha, alpha);
+#pragma unroll 1
+            for (int k = 0; k < D / 32; ++k) {
               uint32_t ra[16];
-              tmem_ld16(lane + tc_.o + k * 16, ra);
+              tmem_ld16(lane + ocol + k * 16, ra);
               tmem_wait_ld16(ra);
 #pragma unroll
-              for (int i = 0; i < 16; ++i) ra[i] = __float_as_uint(__uint_as_float(ra[i]) * alpha);
-              tmem_st16(lane + tc_.o + k * 16, ra);
+              for (int i = 0; i < 8; ++i) {
+                const float2 o2 = f2_unpack(f2_mul(
+                    f2_pack(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1])), a2));
+                ra[2 * i] = __float_as_uint(o2.x);
+                ra[2 * i + 1] = __float_as_uint(o2.y);
+              }
+              tmem_st16(lane + ocol + k * 16, ra);
             }
           }
         }
-        tmem_wait_st();
-        tc_fence_before();
-        mbar_arrive(bar(s, B_PFULL0 + sb));
       }
+      tmem_wait_st();
+      tc_fence_before();
+      mbar_arrive(bar(s, B_PFULL0 + sb));
+    }
+    if (!online) {
+      const float2 a = f2_unpack(f2_add(la, lb));
+      l = a.x + a.y;
     }
 
     // Stage the next tile's Q so its first QK products overlap this epilogue.
     const int nxt = it + static_cast<int>(gridDim.x);
-    if (nxt < n_items && !load_q<D>(s, lane + tc_.q, r, p.tiles[nxt / p.bh].nvalid, qc)) return;
+    if (nxt < n_items &&
+        !load_q<D>(s, lane + tc_.q, wg, r, p.tiles[map_item(p, nxt).tile].nvalid, qc))
+      return;
 
     if (!wait_warp(s, bar(s, B_OFULL), tiles_done & 1u)) return;
+    // the row sum is the sum of the two warpgroups' partial sums
+    const uint32_t lpar = tiles_done & 1u;
     ++tiles_done;
+    s.xch_l[(lpar * 2 + wg) * kTileM + r] = l;
+    if (!xch_sync(s, xc)) return;
+    const float lsum = s.xch_l[(lpar * 2 + 0) * kTileM + r] + s.xch_l[(lpar * 2 + 1) * kTileM + r];
     tc_fence_after();
-    const float inv = 1.f / l;
-    float* orow = p.out + grow * D;
+    const float inv = 1.f / lsum;
+    float* orow = p.out + grow * D + wg * (D / 2);
 #pragma unroll 1
-    for (int k = 0; k < D / 16; ++k) {
+    for (int k = 0; k < D / 32; ++k) {
       uint32_t v[16];
-      tmem_ld16(lane + tc_.o + k * 16, v);
+      tmem_ld16(lane + ocol + k * 16, v);
       tmem_wait_ld16(v);
       if (valid) {
         float4* dst = reinterpret_cast<float4*>(orow + k * 16);
@@ -417,18 +569,21 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
 }
 
 // -------------------------------------------------------------------- kernel
-template <int D>
+// MAXC = 16-column chunks per warpgroup and key step: ceil(G * bk / 32).
+template <int D, int MAXC>
 __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
-  const uint32_t stage_bytes = static_cast<uint32_t>(p.bk) * D * 2u;
+  const uint32_t stage_bytes = static_cast<uint32_t>(p.G * p.bk) * D * 2u;
   Shared s;
   s.q = base;
   s.k = base + kTileM * D * 2;
   s.v = s.k + static_cast<uint32_t>(p.stages_k) * stage_bytes;
   s.bars = s.v + static_cast<uint32_t>(p.stages_v) * stage_bytes;
   uint8_t* gbars = smem_raw + (s.bars - raw);
+  s.xch_m = reinterpret_cast<float*>(gbars + 8 * B_COUNT + 16);
+  s.xch_l = s.xch_m + 2 * 2 * kTileM;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(gbars + 8 * B_COUNT);
   s.abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   s.status = p.status;
@@ -436,14 +591,15 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
 
   if (threadIdx.x == 0) {
     mbar_init(bar(s, B_QFULL), 1);
-    mbar_init(bar(s, B_QEMPTY), kTileM);
-    mbar_init(bar(s, B_QTFULL), kTileM);
+    mbar_init(bar(s, B_QEMPTY), kSoftmaxThreads);
+    mbar_init(bar(s, B_QTFULL), kSoftmaxThreads);
     mbar_init(bar(s, B_OBAR), 1);
     mbar_init(bar(s, B_OFULL), 1);
     for (int i = 0; i < 2; ++i) {
       mbar_init(bar(s, B_SFULL0 + i), 1);
-      mbar_init(bar(s, B_PFULL0 + i), kTileM);
+      mbar_init(bar(s, B_PFULL0 + i), kSoftmaxThreads);
     }
+    mbar_init(bar(s, B_XCH), kSoftmaxThreads);
     for (int i = 0; i < 4; ++i) {
       mbar_init(bar(s, B_KFULL0 + i), 1);
       mbar_init(bar(s, B_KEMPTY0 + i), 1);
@@ -470,9 +626,9 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
   if (warp == 0) {
     if (lane == 0) producer<D>(p, s);
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer<D>(p, s, tbase);
+    if (lane == 0) mma_issuer<D, MAXC>(p, s, tbase);
   } else if (warp >= kSoftmaxWarp0) {
-    softmax_wg<D>(p, s, tbase);
+    softmax_wg<D, MAXC>(p, s, tbase);
   }
 
   tc_fence_before();
@@ -499,38 +655,49 @@ __global__ void timeout_selftest_kernel(long long limit_cycles, int* status) {
   }
 }
 
-}  // namespace
-
-size_t forward_smem_bytes(int D, int bk, int stages_k, int stages_v) {
-  const size_t stage = static_cast<size_t>(bk) * D * 2;
-  return 1024 + static_cast<size_t>(kTileM) * D * 2 + (stages_k + stages_v) * stage +
-         8 * B_COUNT + 16;
+template <int D, int MAXC>
+cudaError_t launch_one(const FwdParams& p, int grid, size_t smem, cudaStream_t stream) {
+  static bool attr_set = false;
+  if (!attr_set) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        wsattn_fwd_kernel<D, MAXC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
+    if (e != cudaSuccess) return e;
+    attr_set = true;
+  }
+  wsattn_fwd_kernel<D, MAXC><<<grid, kThreads, smem, stream>>>(p);
+  return cudaGetLastError();
 }
 
-void forward_stages(int D, int bk, size_t smem_optin, int* stages_k, int* stages_v) {
+template <int D>
+cudaError_t launch_d(const FwdParams& p, int grid, size_t smem, cudaStream_t stream) {
+  switch ((p.G * p.bk + 31) / 32) {
+    case 1: return launch_one<D, 1>(p, grid, smem, stream);
+    case 2: return launch_one<D, 2>(p, grid, smem, stream);
+    case 3: return launch_one<D, 3>(p, grid, smem, stream);
+    case 4: return launch_one<D, 4>(p, grid, smem, stream);
+    case 5: return launch_one<D, 5>(p, grid, smem, stream);
+    default: return cudaErrorInvalidValue;
+  }
+}
+
+}  // namespace
+
+size_t forward_smem_bytes(int D, int step_keys, int stages_k, int stages_v) {
+  const size_t stage = static_cast<size_t>(step_keys) * D * 2;
+  return 1024 + static_cast<size_t>(kTileM) * D * 2 + (stages_k + stages_v) * stage +
+         8 * B_COUNT + 16 + kXchBytes;
+}
+
+void forward_stages(int D, int step_keys, size_t smem_optin, int* stages_k, int* stages_v) {
   int st = 4;
-  while (st > 1 && forward_smem_bytes(D, bk, st, st) > smem_optin) --st;
+  while (st > 1 && forward_smem_bytes(D, step_keys, st, st) > smem_optin) --st;
   *stages_k = st;
   *stages_v = st;
 }
 
 cudaError_t launch_forward(const FwdParams& p, int D, int grid, size_t smem, cudaStream_t stream) {
-  static bool attr_set[2] = {false, false};
-  const int idx = D == 128 ? 1 : 0;
-  cudaError_t e = cudaSuccess;
-  if (!attr_set[idx]) {
-    e = D == 128 ? cudaFuncSetAttribute(wsattn_fwd_kernel<128>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, 232448)
-                 : cudaFuncSetAttribute(wsattn_fwd_kernel<64>,
-                                        cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
-    if (e != cudaSuccess) return e;
-    attr_set[idx] = true;
-  }
-  if (D == 128)
-    wsattn_fwd_kernel<128><<<grid, kThreads, smem, stream>>>(p);
-  else
-    wsattn_fwd_kernel<64><<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  static_assert(kMaxChunksAll * 32 >= kMaxStepKeys, "chunk instantiations must cover a step");
+  return D == 128 ? launch_d<128>(p, grid, smem, stream) : launch_d<64>(p, grid, smem, stream);
 }
 
 cudaError_t launch_timeout_selftest(long long limit_cycles, int* status, cudaStream_t stream) {

@@ -13,19 +13,28 @@ namespace wsattn {
 
 // Rows of one query tile: the M of every tcgen05.mma the forward issues.
 constexpr int kTileM = 128;
-// Largest key block the forward kernel streams (tensor-memory budget:
-// O (D cols) + two S buffers + Q (D/2 cols) within 512 columns).
+// Largest key block, and largest key step, the forward kernel streams
+// (tensor-memory budget: O (D cols) + two S buffers + Q (D/2 cols) within 512
+// columns).  A step is up to floor(160 / bk) consecutive active blocks.
 constexpr int kMaxBlockK = 160;
+constexpr int kMaxStepKeys = 160;
 // Default eligibility threshold, in scaled-logit units.
 constexpr float kDefaultTau = 40.0f;
 
 // One unit of forward work for one (b, h): a 128-row query tile inside one
-// frame and that frame's list of active key blocks.
+// frame and that frame's active key blocks.  A frame's key blocks form at
+// most two runs of consecutive blocks (the reference frames and the window),
+// so the kernel walks them arithmetically: block j is run0 + j for j < len0,
+// else run1 + (j - len0).
 struct WorkTile {
   int32_t row0;    // first query token of the tile (within the head)
   int32_t nvalid;  // rows of the tile that belong to the frame (<= 128)
-  int32_t kbeg;    // [kbeg, kend) indexes the frame's key blocks in kcol
-  int32_t kend;
+  int32_t nblk;    // active key blocks of the frame
+  int32_t run0;    // first key block of the first run (units of bk)
+  int32_t len0;    // blocks in the first run
+  int32_t run1;    // first key block of the second run
+  int32_t nstep;   // key steps: ceil(len0 / G) + ceil((nblk - len0) / G)
+  int32_t kbeg;    // first of the frame's blocks in kcol (kcol[kbeg + j], j < nblk)
 };
 
 // Host-side plan: geometry, block map, and the forward work list.
@@ -37,7 +46,13 @@ struct HostPlan {
   std::vector<int32_t> col;        // [nnz]
   std::vector<WorkTile> tiles;     // longest first
   std::vector<int32_t> kcol;       // per frame, key block indices (units of bk)
+  // Tiles with equal key-list length form a class; class c covers tiles
+  // [cls[c], cls[c + 1]).  The forward visits work items class by class
+  // (longest first) and, inside a class, head by head, so CTAs running at
+  // the same time stream the same head's keys and values.
+  std::vector<int32_t> cls;
   int64_t active_pairs = 0;        // active (query, key) pairs per (b, h)
+  int G = 1;                       // blocks per key step of the forward kernel
 };
 
 // Builds everything above; returns a WSATTN_* status.
@@ -76,7 +91,8 @@ struct FwdParams {
   CUtensorMap tm_k;  // [BH*N, D] bf16, box {64, bk}
   CUtensorMap tm_v;  // [BH*N, D] bf16, box {64, bk}
   const WorkTile* tiles;
-  const int32_t* kcol;
+  const int32_t* cls;    // class boundaries into tiles, n_cls + 1 entries
+  int n_cls;
   const float* m_rows;   // [BH*N] fixed softmax max per row (uncentered logit units)
   const uint8_t* elig;   // [BH]
   float* out;            // [BH*N, D]
@@ -85,15 +101,16 @@ struct FwdParams {
   int bh;                // batch * heads
   int n;                 // tokens per head
   int bk;                // key block rows
+  int G;                 // blocks per full key step (step keys <= kMaxStepKeys)
   int stages_k, stages_v;
   int force_path;        // -1 auto, 0 fixed, 1 online
   float scale_log2;      // softmax scale * log2(e)
 };
 
 // Dynamic shared memory the forward kernel needs for (D, bk, stages).
-size_t forward_smem_bytes(int D, int bk, int stages_k, int stages_v);
+size_t forward_smem_bytes(int D, int step_keys, int stages_k, int stages_v);
 // Largest stage counts (<= 4 each) that fit the per-block shared memory.
-void forward_stages(int D, int bk, size_t smem_optin, int* stages_k, int* stages_v);
+void forward_stages(int D, int step_keys, size_t smem_optin, int* stages_k, int* stages_v);
 // Launches the persistent forward kernel on `grid` CTAs.
 cudaError_t launch_forward(const FwdParams& p, int D, int grid, size_t smem, cudaStream_t s);
 

@@ -58,6 +58,7 @@ int build_host_plan(int frames, int tokens_per_frame, int window, int ref_frames
   p.bq = bq; p.bk = bk; p.N = N;
   p.nqb = N / bq;
   p.nkb = N / bk;
+  p.G = bk <= kMaxStepKeys ? kMaxStepKeys / bk : 1;
   try {
     // Bitmap and CSR.
     p.bitmap.assign(static_cast<size_t>(p.nqb * p.nkb), 0);
@@ -91,20 +92,43 @@ int build_host_plan(int frames, int tokens_per_frame, int window, int ref_frames
            e < p.row_ptr[static_cast<size_t>(qb0 + 1)]; ++e)
         p.kcol.push_back(p.col[static_cast<size_t>(e)]);
       const int32_t kend = static_cast<int32_t>(p.kcol.size());
+      // Split the (increasing) key-block list into runs of consecutive blocks.
+      int32_t run[2] = {0, 0}, len[2] = {0, 0};
+      int nrun = 0;
+      for (int32_t e = kbeg; e < kend; ++e) {
+        const int32_t kb = p.kcol[static_cast<size_t>(e)];
+        if (nrun > 0 && kb == run[nrun - 1] + len[nrun - 1]) {
+          ++len[nrun - 1];
+        } else {
+          if (nrun == 2) return WSATTN_ERR_UNSUPPORTED;  // not produced by this mask family
+          run[nrun] = kb;
+          len[nrun] = 1;
+          ++nrun;
+        }
+      }
+      if (nrun == 0) return WSATTN_ERR_BAD_ARG;  // every frame sees at least itself
       for (int t = 0; t < tiles_per_frame; ++t) {
         WorkTile wt;
         wt.row0 = static_cast<int32_t>(a * T + t * kTileM);
         wt.nvalid = std::min(kTileM, T - t * kTileM);
+        wt.nblk = kend - kbeg;
+        wt.run0 = run[0];
+        wt.len0 = len[0];
+        wt.run1 = nrun == 2 ? run[1] : 0;
+        wt.nstep = (len[0] + p.G - 1) / p.G + (len[1] + p.G - 1) / p.G;
         wt.kbeg = kbeg;
-        wt.kend = kend;
         p.tiles.push_back(wt);
       }
     }
     // Longest first (the reference frame's tiles see every key block); the
     // order among equal lengths stays the token order.
     std::stable_sort(p.tiles.begin(), p.tiles.end(), [](const WorkTile& x, const WorkTile& y) {
-      return (x.kend - x.kbeg) > (y.kend - y.kbeg);
+      return x.nblk > y.nblk;
     });
+    p.cls.push_back(0);
+    for (size_t i = 1; i < p.tiles.size(); ++i)
+      if (p.tiles[i].nblk != p.tiles[i - 1].nblk) p.cls.push_back(static_cast<int32_t>(i));
+    p.cls.push_back(static_cast<int32_t>(p.tiles.size()));
   } catch (const std::bad_alloc&) {
     return WSATTN_ERR_NO_MEMORY;
   }
