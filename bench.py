@@ -38,7 +38,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 # dram__bytes_read.sum + dram__bytes_write.sum of one forward launch, from an
 # ncu capture, keyed by workload; valid only for the kernel source it was
 # measured on (sha256 of forward.cu, first 16 hex digits).
-FORWARD_TRAFFIC = {}
+FORWARD_TRAFFIC = {
+    ("sr", 80, "7d4c9915f03b0008"): 1.219e9,
+}
 
 
 def _peaks():
@@ -359,6 +361,8 @@ def run_gpu(args, wl, world, rank, local):
         "roofline": {"bound": "tensor", "kernel": "wsattn_fwd_kernel", "achieved": achieved,
                      "peak": peaks["bf16_tflops"], "unit": "TFLOP/s",
                      "frac": achieved / peaks["bf16_tflops"], "traffic": traffic,
+                     "traffic_unit": "bytes per launch (ncu dram read + write)",
+                     "algorithmic_bytes": 3 * elem * 2 + elem * 4,
                      "peak_source": f"{peaks['source']} (bf16 burst)",
                      "ms_per_launch": fwd_avg},
         "prepare": {"bound": "hbm", "ms_per_call": prep_avg, "launches": 3,
