@@ -59,8 +59,9 @@ struct HostPlan {
 int build_host_plan(int frames, int tokens_per_frame, int window, int ref_frames, int heads,
                     int head_dim, int block_q, int block_k, HostPlan* out);
 
-// Picks a block size for T: the largest valid size <= 128 if it is >= 48,
-// else the largest valid size <= 160 (valid: multiple of 16 dividing T).
+// Picks a block size for T: among the valid sizes (multiples of 16 dividing
+// T, at most 160), the one whose forward key step floor(160 / bk) * bk is
+// longest, the larger on ties.
 int auto_block(int T);
 
 // ------------------------------------------------------------ prepare

@@ -19,14 +19,20 @@ namespace wsattn {
 
 static bool valid_block(int b, int T) { return b >= 16 && b % 16 == 0 && T % b == 0; }
 
+// The forward kernel streams keys in steps of floor(160 / bk) blocks, so the
+// automatic size is the valid block whose step holds the most keys (ties go
+// to the larger block: fewer TMA boxes per step).
 int auto_block(int T) {
-  int best128 = 0, best_max = 0;
+  int best = 0, best_step = 0;
   for (int b = 16; b <= kMaxBlockK && b <= T; b += 16) {
     if (T % b != 0) continue;
-    if (b <= 128) best128 = b;
-    best_max = b;
+    const int step = (kMaxStepKeys / b) * b;
+    if (step >= best_step) {
+      best = b;
+      best_step = step;
+    }
   }
-  return best128 >= 48 ? best128 : best_max;
+  return best;
 }
 
 static bool frames_interact(int a, int c, int w, int R) {

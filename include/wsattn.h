@@ -71,10 +71,12 @@ typedef struct wsattn_plan_s* wsattn_plan_t;
  *   heads             H >= 1
  *   head_dim          D; the kernels implement 64 and 128
  *   block_q, block_k  block sizes of the map: multiples of 16 dividing T, or
- *                     0 to let the plan choose (the largest valid size <= 128
- *                     if it is >= 48, else the largest valid size <= 160).
- *                     The forward kernel streams keys in block_k rows, so
- *                     block_k must be <= 160 for wsattn_forward.
+ *                     0 to let the plan choose.  The forward kernel streams
+ *                     keys in steps of floor(160 / block_k) consecutive
+ *                     active blocks, so block_k must be <= 160 for
+ *                     wsattn_forward; the automatic size is the valid size
+ *                     (<= 160) whose step holds the most keys, the larger
+ *                     size on ties.
  *   out               receives the plan handle (owned by the caller; release
  *                     with wsattn_plan_destroy).
  * Errors: BAD_ARG (sizes, null out), BAD_BLOCK, UNSUPPORTED (head_dim),

@@ -83,7 +83,8 @@ def test_plan_matches_oracle_edge_shapes(case):
 
 def test_auto_block_sizes():
     import frame_aligned_window_gb300 as fw
-    expect = {"tiny": 48, "small": 16, "sr": 80, "sr_long": 80, "dense": 112}
+    # longest forward step floor(160 / bk) * bk, larger bk on ties
+    expect = {"tiny": 16, "small": 16, "sr": 80, "sr_long": 160, "dense": 32}
     for name, bk in expect.items():
         wl = WORKLOADS[name]
         plan = fw.wsattn_plan(wl.frames, wl.tokens_per_frame, wl.window, wl.ref_frames,

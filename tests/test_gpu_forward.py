@@ -131,6 +131,25 @@ def test_block_sizes_sr_long_shape_small(bk):
     _check(got, want, f"bk={bk}")
 
 
+@pytest.mark.parametrize("bk", [32, 112, 224])
+def test_block_sizes_dense_frame_span(bk):
+    # T = 224 admits 16, 32, 112 and 224: key steps of 160 (5 x 32) and 112
+    # keys, and a block above the kernel's step limit (rejected by forward)
+    import frame_aligned_window_gb300 as fw
+    wl, q, k, v = micro(42, 1, 2, 128, 4, 1, 224, 4)
+    if bk > 160:
+        plan = fw.wsattn_plan(wl.frames, wl.tokens_per_frame, wl.window, wl.ref_frames,
+                              wl.heads, wl.head_dim, 0, bk)
+        qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+        fw.wsattn_prepare(plan, qd, kd)
+        with pytest.raises(fw.WsattnError) as e:
+            fw.wsattn_forward(plan, qd, kd, vd)
+        assert e.value.code == 3
+        return
+    _, out, _ = gpu_run(wl, q, k, v, block_k=bk)
+    _full_compare(wl, q, k, v, out)
+
+
 @pytest.mark.parametrize("case", [
     # seed, B, H, D, F, R, T, w: edge shapes
     (51, 1, 1, 128, 1, 0, 16, 0),      # one frame of 16 tokens (single block, ragged tile)
