@@ -16,7 +16,7 @@
 // Persistent kernel, one CTA per SM, 12 warps:
 //   warp 0      TMA producer: Q tile (128 x D) into a staging buffer; K and V
 //               steps into two rings, all 128-byte swizzled.
-//   warp 1      MMA issuer (one thread): S = Q K^T and O += P V with
+//   warps 1, 3  MMA issuers (one thread each): S = Q K^T and O += P V with
 //               tcgen05.mma kind::f16 (bf16 in, fp32 accumulate in TMEM).
 //               Q and P are read from TMEM, K and V from shared memory.
 //   warp 2      allocates and frees tensor memory.
@@ -78,6 +78,8 @@ enum : int {
   B_PFULL0,      // softmax -> MMA: P buffer 0 / 1 written
   B_PFULL1,
   B_XCH,         // softmax <-> softmax: row maxima / row sums exchanged
+  B_PVDONE0,     // PV issuer -> QK issuer: PV that read S buffer 0 / 1 done
+  B_PVDONE1,
   B_KFULL0,
   B_KEMPTY0 = B_KFULL0 + 4,
   B_VFULL0 = B_KEMPTY0 + 4,
@@ -263,12 +265,70 @@ __device__ void producer(const FwdParams& p, const Shared& s) {
   }
 }
 
-// ---------------------------------------------------------------- MMA issuer
-// One thread.  Descriptor bases are computed once; each MMA adds a constant
-// to the start-address field (bits 0-13, address >> 4), and both k-step loops
-// are unrolled, so the thread spends a few instructions per MMA.
+// ---------------------------------------------------------------- MMA issue
+// Two single-thread issuers feed the tensor core: warp 1 issues S = Q K^T,
+// warp 3 issues O += P V.  A tcgen05.mma blocks its issuing thread while the
+// MMA queue is full, so with one issuer every barrier wait and every bit of
+// bookkeeping between MMA groups left the tensor core idle; with two, one
+// issuer's waits overlap the other's MMAs.  The only hazard between them is
+// the S buffer: QK into buffer b overwrites the P that the previous PV from
+// buffer b reads, so the QK issuer waits on that PV's commit (pv_done[b]).
+// Descriptor bases are computed once; each MMA adds a constant to the
+// start-address field (bits 0-13, address >> 4), and the k-step loops are
+// unrolled.
+template <int D>
+__device__ void qk_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
+  constexpr int kBoxes = D / 64;
+  const int bk = p.bk, G = p.G;
+  const int ns = G * bk;
+  const uint32_t box_pitch = static_cast<uint32_t>(ns) * 128u;
+  const uint32_t stage_bytes = box_pitch * kBoxes;
+  const TmemCols tc_ = tmem_cols<D>(ns);
+  const uint32_t t_s0 = tbase + tc_.s0, t_s1 = tbase + tc_.s1, t_q = tbase + tc_.q;
+  const uint32_t id_qk0 = idesc_bf16_f32(kTileM, 0, false);  // N filled per step
+  // K is K-major (SBO 1 KB)
+  const uint64_t kdesc0 = sdesc_sw128(s.k, 16, 1024);
+  const uint64_t box16 = box_pitch >> 4, stage16 = stage_bytes >> 4;
+  const int n_items = p.n_tiles * p.bh;
+  const uint32_t nk = static_cast<uint32_t>(p.stages_k);
+  Ring kr;
+  uint32_t use0 = 0, use1 = 0, tiles_done = 0;  // writes of each S buffer so far
+  Steps qs;
+  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+    const Item im = map_item(p, it);
+    const WorkTile t = p.tiles[im.tile];
+    qs.init(t);
+    if (!wait(s, bar(s, B_QTFULL), tiles_done & 1u, kStatusTimeoutMma)) return;
+    tc_fence_after();
+    for (int j = 0; j < t.nstep; ++j) {
+      const int sb = j & 1;
+      uint32_t& use = sb ? use1 : use0;
+      if (use > 0 &&
+          !wait(s, bar(s, B_PVDONE0 + sb), (use - 1u) & 1u, kStatusTimeoutMma))
+        return;
+      ++use;
+      int nb;
+      qs.next(G, nb);
+      const uint32_t keys = static_cast<uint32_t>(nb * bk);
+      const uint32_t slot = kr.slot;
+      if (!wait(s, bar(s, B_KFULL0 + slot), kr.phase, kStatusTimeoutMma)) return;
+      tc_fence_after();
+      const uint64_t kd = kdesc0 + slot * stage16;
+      const uint32_t d_s = sb ? t_s1 : t_s0;
+      const uint32_t id = id_qk0 | ((keys >> 3) << 17);
+#pragma unroll
+      for (int kk = 0; kk < D / 16; ++kk)
+        mma_ts(d_s, t_q + kk * 8, kd + (kk / 4) * box16 + (kk % 4) * 2, id, kk > 0 ? 1u : 0u);
+      tc_commit(bar(s, B_KEMPTY0 + slot));
+      tc_commit(bar(s, B_SFULL0 + sb));
+      kr.next(nk);
+    }
+    ++tiles_done;
+  }
+}
+
 template <int D, int MAXC>
-__device__ void mma_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
+__device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
   constexpr int kBoxes = D / 64;
   const int bk = p.bk, G = p.G;
   const int ns = G * bk;
@@ -276,50 +336,21 @@ __device__ void mma_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) 
   const uint32_t stage_bytes = box_pitch * kBoxes;
   const TmemCols tc_ = tmem_cols<D>(ns);
   const uint32_t t_o = tbase + tc_.o, t_s0 = tbase + tc_.s0, t_s1 = tbase + tc_.s1;
-  const uint32_t t_q = tbase + tc_.q;
-  const uint32_t id_qk0 = idesc_bf16_f32(kTileM, 0, false);  // N filled per step
   const uint32_t id_pv = idesc_bf16_f32(kTileM, D, true);
-  // K is K-major (SBO 1 KB); V is MN-major (LBO = the 64-column box pitch).
-  const uint64_t kdesc0 = sdesc_sw128(s.k, 16, 1024);
+  // V is MN-major (LBO = the 64-column box pitch)
   const uint64_t vdesc0 = sdesc_sw128(s.v, box_pitch, 1024);
-  const uint64_t box16 = box_pitch >> 4, stage16 = stage_bytes >> 4;
+  const uint64_t stage16 = stage_bytes >> 4;
   const int n_items = p.n_tiles * p.bh;
-  const uint32_t nk = static_cast<uint32_t>(p.stages_k), nv = static_cast<uint32_t>(p.stages_v);
-  Ring kr, vr;
-  uint32_t pc0 = 0, pc1 = 0, tiles_done = 0;
-  Steps qs, ps;
-
-  // S(j) = Q K_j^T into S buffer (j & 1).
-  auto issue_qk = [&](int j) -> bool {
-    int nb;
-    qs.next(G, nb);
-    const uint32_t keys = static_cast<uint32_t>(nb * bk);
-    const uint32_t slot = kr.slot;
-    if (!wait(s, bar(s, B_KFULL0 + slot), kr.phase, kStatusTimeoutMma)) return false;
-    tc_fence_after();
-    const uint64_t kd = kdesc0 + slot * stage16;
-    const uint32_t d_s = (j & 1) ? t_s1 : t_s0;
-    const uint32_t id = id_qk0 | ((keys >> 3) << 17);
-#pragma unroll
-    for (int kk = 0; kk < D / 16; ++kk)
-      mma_ts(d_s, t_q + kk * 8, kd + (kk / 4) * box16 + (kk % 4) * 2, id, kk > 0 ? 1u : 0u);
-    tc_commit(bar(s, B_KEMPTY0 + slot));
-    tc_commit(bar(s, (j & 1) ? B_SFULL1 : B_SFULL0));
-    kr.next(nk);
-    return true;
-  };
-
+  const uint32_t nv = static_cast<uint32_t>(p.stages_v);
+  Ring vr;
+  uint32_t pc0 = 0, pc1 = 0;
+  Steps ps;
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     const Item im = map_item(p, it);
     const WorkTile t = p.tiles[im.tile];
     const int nstep = t.nstep;
     const bool online = p.force_path >= 0 ? (p.force_path == 1) : (p.elig[im.bh] == 0);
-    qs.init(t);
     ps.init(t);
-    if (!wait(s, bar(s, B_QTFULL), tiles_done & 1u, kStatusTimeoutMma)) return;
-    tc_fence_after();
-    for (int j = 0; j < nstep && j < 2; ++j)
-      if (!issue_qk(j)) return;
     for (int j = 0; j < nstep; ++j) {
       int nb;
       ps.next(G, nb);
@@ -340,12 +371,11 @@ __device__ void mma_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) 
       for (int kk = 1; kk < 2 * MAXC; ++kk)
         if (kk < nks) mma_ts(t_o, a_p + kk * 8, vd + kk * 128, id_pv, 1u);
       tc_commit(bar(s, B_VEMPTY0 + vslot));
+      tc_commit(bar(s, B_PVDONE0 + sb));
       vr.next(nv);
       if (online && j + 1 < nstep) tc_commit(bar(s, B_OBAR));
-      if (j + 2 < nstep && !issue_qk(j + 2)) return;
     }
     tc_commit(bar(s, B_OFULL));
-    ++tiles_done;
   }
 }
 
@@ -600,6 +630,8 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
       mbar_init(bar(s, B_PFULL0 + i), kSoftmaxThreads);
     }
     mbar_init(bar(s, B_XCH), kSoftmaxThreads);
+    mbar_init(bar(s, B_PVDONE0), 1);
+    mbar_init(bar(s, B_PVDONE1), 1);
     for (int i = 0; i < 4; ++i) {
       mbar_init(bar(s, B_KFULL0 + i), 1);
       mbar_init(bar(s, B_KEMPTY0 + i), 1);
@@ -626,7 +658,9 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
   if (warp == 0) {
     if (lane == 0) producer<D>(p, s);
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer<D, MAXC>(p, s, tbase);
+    if (lane == 0) qk_issuer<D>(p, s, tbase);
+  } else if (warp == 3) {
+    if (lane == 0) pv_issuer<D, MAXC>(p, s, tbase);
   } else if (warp >= kSoftmaxWarp0) {
     softmax_wg<D, MAXC>(p, s, tbase);
   }
