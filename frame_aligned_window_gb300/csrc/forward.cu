@@ -26,20 +26,22 @@
 //               (s = 16 * ceil(keys / 32)), so each SMSP runs two softmax warps.
 //
 // Keys are consumed in steps of up to G consecutive active blocks of one run
-// (G * bk <= 160 keys): one TMA box per block lands in consecutive rows of the
-// step's stage (the swizzle pattern continues across boxes), and each MMA
-// covers the whole step, so the per-step handoffs (barrier waits, commits,
-// softmax rounds) are amortised over up to 160 keys.
+// (G * bk <= 160 keys): one TMA box per block lands
+// in consecutive rows of the step's stage (the swizzle pattern continues
+// across boxes), and each MMA covers the whole step.
 //
-// Tensor memory (512 columns): O [0, D), S0/S1 double buffer of G*bk columns
-// each, Q (D/2 columns of bf16 pairs).  P (keys/2 columns of bf16 pairs)
-// aliases its S buffer from column s/2: warpgroup 0's half lands in columns
-// [s/2, s) and warpgroup 1's in [s, s/2 + keys/2).  Warpgroup 0 walks its
-// 16-column chunks backwards and warpgroup 1 forwards, so every chunk's P
-// lands in S columns its own warpgroup has already read: the two never wait
-// on each other in the fixed-max path, and each holds one chunk (plus the
-// next one in flight) in registers.  While the softmax works on S(j), the
-// tensor core runs PV(j-1) and QK(j+1).
+// Tensor memory (512 columns): O [0, D), ns S buffers of `step` columns each
+// (two of 160 at D = 128; three or four for shorter steps), then Q (D/2
+// columns of bf16 pairs).  P
+// (keys/2 columns of bf16 pairs) aliases its S buffer from column s/2:
+// warpgroup 0's half lands in columns [s/2, s) and warpgroup 1's in
+// [s, s/2 + keys/2).  Warpgroup 0 walks its 16-column chunks backwards and
+// warpgroup 1 forwards, so every chunk's P lands in S columns its own
+// warpgroup has already read: the two never wait on each other in the
+// fixed-max path, and each holds one chunk (plus the next one in flight) in
+// registers.  The QK^T that refills a buffer waits for the PV that read its
+// P, ns steps back; while the softmax works on S(j) the tensor core runs
+// PV(j-1) and QK^T(j+1 .. j+ns-1).
 //
 // Work items (tile, b*h) go class by class (tiles with equal key lists,
 // longest first) and head by head inside a class, so the CTAs running at one
@@ -60,7 +62,7 @@ using namespace ptx;
 
 constexpr int kThreads = 384;
 constexpr int kSoftmaxWarp0 = 4;
-constexpr int kSoftmaxThreads = 256;
+constexpr int kSoftmaxWarps = 8;
 constexpr int kMaxChunksAll = 5;  // 16-column chunks a warpgroup takes at 160 keys
 constexpr long long kWaitLimitCycles = 1LL << 31;  // about one second
 constexpr float kLog2e = 1.4426950408889634f;
@@ -73,14 +75,11 @@ enum : int {
   B_QTFULL,      // softmax -> MMA: Q tile in TMEM
   B_OBAR,        // MMA -> softmax: PV(j) done (online path only)
   B_OFULL,       // MMA -> softmax: last PV of the tile done
-  B_SFULL0,      // MMA -> softmax: S buffer 0 / 1 written
-  B_SFULL1,
-  B_PFULL0,      // softmax -> MMA: P buffer 0 / 1 written
-  B_PFULL1,
   B_XCH,         // softmax <-> softmax: row maxima / row sums exchanged
-  B_PVDONE0,     // PV issuer -> QK issuer: PV that read S buffer 0 / 1 done
-  B_PVDONE1,
-  B_KFULL0,
+  B_SFULL0,                       // MMA -> softmax: S buffer i written
+  B_PFULL0 = B_SFULL0 + kMaxSBuf,  // softmax -> MMA: P in S buffer i written
+  B_PVDONE0 = B_PFULL0 + kMaxSBuf, // PV issuer -> QK issuer: PV that read buffer i done
+  B_KFULL0 = B_PVDONE0 + kMaxSBuf,
   B_KEMPTY0 = B_KFULL0 + 4,
   B_VFULL0 = B_KEMPTY0 + 4,
   B_VEMPTY0 = B_VFULL0 + 4,
@@ -127,11 +126,22 @@ __device__ __forceinline__ bool wait_warp(const Shared& s, uint32_t b, uint32_t 
   return __all_sync(0xffffffffu, ok);
 }
 
-// Barrier of the two softmax warpgroups (all 256 threads arrive, then wait
-// for the phase), bounded like every other wait; the arrive publishes the
+// Arrival of one softmax warp: the warp's threads synchronise (ordering
+// every lane's prior shared-memory writes and fenced tcgen05 operations
+// before it) and lane 0 arrives.  Barriers the softmax warps signal count
+// one arrival per warp: 256 arrivals on one mbarrier serialise in the
+// shared-memory atomic unit and stall the warps' next barrier operation for
+// hundreds of cycles.
+__device__ __forceinline__ void warp_arrive(uint32_t b) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(b);
+}
+
+// Barrier of the two softmax warpgroups (every warp arrives, then waits for
+// the phase), bounded like every other wait; the arrival publishes the
 // exchange values written before it.
 __device__ __forceinline__ bool xch_sync(const Shared& s, uint32_t& xc) {
-  mbar_arrive(bar(s, B_XCH));
+  warp_arrive(bar(s, B_XCH));
   const bool ok = wait_warp(s, bar(s, B_XCH), xc & 1u);
   ++xc;
   return ok;
@@ -140,15 +150,17 @@ __device__ __forceinline__ bool xch_sync(const Shared& s, uint32_t& xc) {
 // First S column of warpgroup 1 in a step of `keys` keys; P starts at s/2.
 __device__ __forceinline__ int split_col(int keys) { return 16 * ((keys / 16 + 1) / 2); }
 
+// Tensor-memory columns: O [0, D), ns S buffers of `step` columns from D,
+// then Q (D/2 columns).
 struct TmemCols {
-  uint32_t o, s0, s1, q;
+  uint32_t o, s, stride, q;
 };
 
 template <int D>
-__device__ __forceinline__ TmemCols tmem_cols(int step_keys) {
-  const uint32_t spad = (static_cast<uint32_t>(step_keys) + 31u) & ~31u;
-  return TmemCols{0u, static_cast<uint32_t>(D), static_cast<uint32_t>(D) + spad,
-                  static_cast<uint32_t>(D) + 2u * spad};
+__device__ __forceinline__ TmemCols tmem_cols(int step_keys, int ns) {
+  const uint32_t st = static_cast<uint32_t>(step_keys);
+  return TmemCols{0u, static_cast<uint32_t>(D), st,
+                  static_cast<uint32_t>(D) + static_cast<uint32_t>(ns) * st};
 }
 
 struct Item {
@@ -283,16 +295,16 @@ __device__ void qk_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
   const int ns = G * bk;
   const uint32_t box_pitch = static_cast<uint32_t>(ns) * 128u;
   const uint32_t stage_bytes = box_pitch * kBoxes;
-  const TmemCols tc_ = tmem_cols<D>(ns);
-  const uint32_t t_s0 = tbase + tc_.s0, t_s1 = tbase + tc_.s1, t_q = tbase + tc_.q;
+  const TmemCols tc_ = tmem_cols<D>(ns, p.ns);
+  const uint32_t t_s = tbase + tc_.s, t_q = tbase + tc_.q;
   const uint32_t id_qk0 = idesc_bf16_f32(kTileM, 0, false);  // N filled per step
   // K is K-major (SBO 1 KB)
   const uint64_t kdesc0 = sdesc_sw128(s.k, 16, 1024);
   const uint64_t box16 = box_pitch >> 4, stage16 = stage_bytes >> 4;
   const int n_items = p.n_tiles * p.bh;
-  const uint32_t nk = static_cast<uint32_t>(p.stages_k);
-  Ring kr;
-  uint32_t use0 = 0, use1 = 0, tiles_done = 0;  // writes of each S buffer so far
+  const uint32_t nk = static_cast<uint32_t>(p.stages_k), nsb = static_cast<uint32_t>(p.ns);
+  Ring kr, sr;
+  uint32_t tiles_done = 0;
   Steps qs;
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     const Item im = map_item(p, it);
@@ -301,12 +313,9 @@ __device__ void qk_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
     if (!wait(s, bar(s, B_QTFULL), tiles_done & 1u, kStatusTimeoutMma)) return;
     tc_fence_after();
     for (int j = 0; j < t.nstep; ++j) {
-      const int sb = j & 1;
-      uint32_t& use = sb ? use1 : use0;
-      if (use > 0 &&
-          !wait(s, bar(s, B_PVDONE0 + sb), (use - 1u) & 1u, kStatusTimeoutMma))
-        return;
-      ++use;
+      // the PV that last read this S buffer (its P) must be done
+      const uint32_t sb = sr.slot;
+      if (!wait(s, bar(s, B_PVDONE0 + sb), sr.phase ^ 1u, kStatusTimeoutMma)) return;
       int nb;
       qs.next(G, nb);
       const uint32_t keys = static_cast<uint32_t>(nb * bk);
@@ -314,7 +323,7 @@ __device__ void qk_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
       if (!wait(s, bar(s, B_KFULL0 + slot), kr.phase, kStatusTimeoutMma)) return;
       tc_fence_after();
       const uint64_t kd = kdesc0 + slot * stage16;
-      const uint32_t d_s = sb ? t_s1 : t_s0;
+      const uint32_t d_s = t_s + sb * tc_.stride;
       const uint32_t id = id_qk0 | ((keys >> 3) << 17);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
@@ -322,6 +331,7 @@ __device__ void qk_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
       tc_commit(bar(s, B_KEMPTY0 + slot));
       tc_commit(bar(s, B_SFULL0 + sb));
       kr.next(nk);
+      sr.next(nsb);
     }
     ++tiles_done;
   }
@@ -334,16 +344,15 @@ __device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
   const int ns = G * bk;
   const uint32_t box_pitch = static_cast<uint32_t>(ns) * 128u;
   const uint32_t stage_bytes = box_pitch * kBoxes;
-  const TmemCols tc_ = tmem_cols<D>(ns);
-  const uint32_t t_o = tbase + tc_.o, t_s0 = tbase + tc_.s0, t_s1 = tbase + tc_.s1;
+  const TmemCols tc_ = tmem_cols<D>(ns, p.ns);
+  const uint32_t t_o = tbase + tc_.o, t_s = tbase + tc_.s;
   const uint32_t id_pv = idesc_bf16_f32(kTileM, D, true);
   // V is MN-major (LBO = the 64-column box pitch)
   const uint64_t vdesc0 = sdesc_sw128(s.v, box_pitch, 1024);
   const uint64_t stage16 = stage_bytes >> 4;
   const int n_items = p.n_tiles * p.bh;
-  const uint32_t nv = static_cast<uint32_t>(p.stages_v);
-  Ring vr;
-  uint32_t pc0 = 0, pc1 = 0;
+  const uint32_t nv = static_cast<uint32_t>(p.stages_v), nsb = static_cast<uint32_t>(p.ns);
+  Ring vr, pr;
   Steps ps;
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
     const Item im = map_item(p, it);
@@ -356,15 +365,13 @@ __device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
       ps.next(G, nb);
       const int keys = nb * bk;
       const int nks = keys / 16;
-      const int sb = j & 1;
-      uint32_t par;
-      if (sb) { par = pc1 & 1u; ++pc1; } else { par = pc0 & 1u; ++pc0; }
-      if (!wait(s, bar(s, B_PFULL0 + sb), par, kStatusTimeoutMma)) return;
+      const uint32_t sb = pr.slot;
+      if (!wait(s, bar(s, B_PFULL0 + sb), pr.phase, kStatusTimeoutMma)) return;
       const uint32_t vslot = vr.slot;
       if (!wait(s, bar(s, B_VFULL0 + vslot), vr.phase, kStatusTimeoutMma)) return;
       tc_fence_after();
       const uint64_t vd = vdesc0 + vslot * stage16;
-      const uint32_t a_p = (sb ? t_s1 : t_s0) + static_cast<uint32_t>(split_col(keys) / 2);
+      const uint32_t a_p = t_s + sb * tc_.stride + static_cast<uint32_t>(split_col(keys) / 2);
       // 16 key rows (2 KB of V) per k-step
       mma_ts(t_o, a_p, vd, id_pv, j > 0 ? 1u : 0u);
 #pragma unroll
@@ -373,6 +380,7 @@ __device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
       tc_commit(bar(s, B_VEMPTY0 + vslot));
       tc_commit(bar(s, B_PVDONE0 + sb));
       vr.next(nv);
+      pr.next(nsb);
       if (online && j + 1 < nstep) tc_commit(bar(s, B_OBAR));
     }
     tc_commit(bar(s, B_OFULL));
@@ -406,8 +414,8 @@ __device__ bool load_q(const Shared& s, uint32_t t_q, int wg, int r, int nvalid,
   }
   tmem_wait_st();
   tc_fence_before();
-  mbar_arrive(bar(s, B_QTFULL));
-  mbar_arrive(bar(s, B_QEMPTY));
+  warp_arrive(bar(s, B_QTFULL));
+  warp_arrive(bar(s, B_QEMPTY));
   return true;
 }
 
@@ -462,6 +470,17 @@ __device__ __forceinline__ void step_exp(uint32_t sa, uint32_t pa, int n16, bool
   }
 }
 
+// Full steps (n16 == MAXC) run the chunk loop with a compile-time count:
+// without the per-chunk guards the loop is about a quarter faster.
+template <int MAXC>
+__device__ __forceinline__ void step_exp_n(uint32_t sa, uint32_t pa, int n16, bool reverse,
+                                           uint64_t c2, uint64_t nb2, uint64_t& la, uint64_t& lb) {
+  if (n16 == MAXC)
+    step_exp<MAXC>(sa, pa, MAXC, reverse, c2, nb2, la, lb);
+  else
+    step_exp<MAXC>(sa, pa, n16, reverse, c2, nb2, la, lb);
+}
+
 template <int D, int MAXC>
 __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) {
   const int warp = threadIdx.x / 32;
@@ -469,12 +488,14 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
   const int r = (threadIdx.x - kSoftmaxWarp0 * 32) % kTileM;  // tile row == TMEM lane
   const uint32_t lane = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const int bk = p.bk, G = p.G;
-  const TmemCols tc_ = tmem_cols<D>(G * bk);
+  const TmemCols tc_ = tmem_cols<D>(G * bk, p.ns);
   const uint32_t ocol = tc_.o + static_cast<uint32_t>(wg * (D / 2));  // this WG's O half
   const float c = p.scale_log2;
   const uint64_t c2 = f2_pack(c, c);
   const int n_items = p.n_tiles * p.bh;
-  uint32_t qc = 0, sc0 = 0, sc1 = 0, oc = 0, tiles_done = 0, xpar = 0, xc = 0;
+  const uint32_t nsb = static_cast<uint32_t>(p.ns);
+  uint32_t qc = 0, oc = 0, tiles_done = 0, xpar = 0, xc = 0;
+  Ring sr;
 
   int it = blockIdx.x;
   if (it >= n_items) return;
@@ -499,15 +520,13 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
       const uint32_t c0 = wg == 0 ? 0u : static_cast<uint32_t>(split);  // first S column
       const int n16 = (wg == 0 ? split : keys - split) / 16;           // 16-column chunks
       const uint32_t pcol = static_cast<uint32_t>(split / 2) + c0 / 2;  // first P column
-      const int sb = j & 1;
-      uint32_t par;
-      if (sb) { par = sc1 & 1u; ++sc1; } else { par = sc0 & 1u; ++sc0; }
-      if (!wait_warp(s, bar(s, B_SFULL0 + sb), par)) return;
+      const uint32_t sb = sr.slot;
+      if (!wait_warp(s, bar(s, B_SFULL0 + sb), sr.phase)) return;
       tc_fence_after();
-      const uint32_t sbase = lane + (sb ? tc_.s1 : tc_.s0);
+      const uint32_t sbase = lane + tc_.s + sb * tc_.stride;
       if (!online) {
-        step_exp<MAXC>(sbase + c0, sbase + pcol, n16, wg == 0, c2, f2_pack(nb_fixed, nb_fixed), la,
-                       lb);
+        step_exp_n<MAXC>(sbase + c0, sbase + pcol, n16, wg == 0, c2, f2_pack(nb_fixed, nb_fixed), la,
+                         lb);
       } else {
         // row max of this step over both warpgroups' columns, one chunk at a time
         float mx = -INFINITY;
@@ -525,8 +544,8 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         const float m_new = fmaxf(m, fmaxf(mx, mo) * c);
         const float alpha = ex2_approx(m - m_new);
         uint64_t sa2 = f2_pack(0.f, 0.f), sb2 = sa2;
-        step_exp<MAXC>(sbase + c0, sbase + pcol, n16, wg == 0, c2, f2_pack(-m_new, -m_new), sa2,
-                       sb2);
+        step_exp_n<MAXC>(sbase + c0, sbase + pcol, n16, wg == 0, c2, f2_pack(-m_new, -m_new), sa2,
+                         sb2);
         const float2 a = f2_unpack(f2_add(sa2, sb2));
         l = l * alpha + (a.x + a.y);
         m = m_new;
@@ -556,7 +575,8 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
       }
       tmem_wait_st();
       tc_fence_before();
-      mbar_arrive(bar(s, B_PFULL0 + sb));
+      warp_arrive(bar(s, B_PFULL0 + sb));
+      sr.next(nsb);
     }
     if (!online) {
       const float2 a = f2_unpack(f2_add(la, lb));
@@ -621,17 +641,16 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
 
   if (threadIdx.x == 0) {
     mbar_init(bar(s, B_QFULL), 1);
-    mbar_init(bar(s, B_QEMPTY), kSoftmaxThreads);
-    mbar_init(bar(s, B_QTFULL), kSoftmaxThreads);
+    mbar_init(bar(s, B_QEMPTY), kSoftmaxWarps);
+    mbar_init(bar(s, B_QTFULL), kSoftmaxWarps);
     mbar_init(bar(s, B_OBAR), 1);
     mbar_init(bar(s, B_OFULL), 1);
-    for (int i = 0; i < 2; ++i) {
+    for (int i = 0; i < kMaxSBuf; ++i) {
       mbar_init(bar(s, B_SFULL0 + i), 1);
-      mbar_init(bar(s, B_PFULL0 + i), kSoftmaxThreads);
+      mbar_init(bar(s, B_PFULL0 + i), kSoftmaxWarps);
+      mbar_init(bar(s, B_PVDONE0 + i), 1);
     }
-    mbar_init(bar(s, B_XCH), kSoftmaxThreads);
-    mbar_init(bar(s, B_PVDONE0), 1);
-    mbar_init(bar(s, B_PVDONE1), 1);
+    mbar_init(bar(s, B_XCH), kSoftmaxWarps);
     for (int i = 0; i < 4; ++i) {
       mbar_init(bar(s, B_KFULL0 + i), 1);
       mbar_init(bar(s, B_KEMPTY0 + i), 1);
@@ -730,7 +749,7 @@ void forward_stages(int D, int step_keys, size_t smem_optin, int* stages_k, int*
 }
 
 cudaError_t launch_forward(const FwdParams& p, int D, int grid, size_t smem, cudaStream_t stream) {
-  static_assert(kMaxChunksAll * 32 >= kMaxStepKeys, "chunk instantiations must cover a step");
+  static_assert(kMaxChunksAll * 32 >= kStepKeys, "chunk instantiations must cover a step");
   return D == 128 ? launch_d<128>(p, grid, smem, stream) : launch_d<64>(p, grid, smem, stream);
 }
 

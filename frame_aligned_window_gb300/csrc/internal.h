@@ -13,11 +13,20 @@ namespace wsattn {
 
 // Rows of one query tile: the M of every tcgen05.mma the forward issues.
 constexpr int kTileM = 128;
-// Largest key block, and largest key step, the forward kernel streams
-// (tensor-memory budget: O (D cols) + two S buffers + Q (D/2 cols) within 512
-// columns).  A step is up to floor(160 / bk) consecutive active blocks.
+// Largest key block, and the key step the plan aims for: floor(160 / bk)
+// blocks (one block when bk > 160 is rejected by the forward).
 constexpr int kMaxBlockK = 160;
-constexpr int kMaxStepKeys = 160;
+constexpr int kStepKeys = 160;
+// Tensor memory (512 columns) holds O (D columns), Q (D/2 columns) and the S
+// buffers the forward rotates through: two of 160 columns at D = 128, three
+// of up to 106, four of up to 80.  The QK^T that refills a buffer waits for
+// the PV that read its P, ns steps back.
+constexpr int kTmemColumns = 512;
+constexpr int kMaxSBuf = 4;
+inline int forward_s_buffers(int D, int step_keys) {
+  const int n = (kTmemColumns - D - D / 2) / step_keys;
+  return n > kMaxSBuf ? kMaxSBuf : n;
+}
 // Default eligibility threshold, in scaled-logit units.
 constexpr float kDefaultTau = 40.0f;
 
@@ -60,8 +69,8 @@ int build_host_plan(int frames, int tokens_per_frame, int window, int ref_frames
                     int head_dim, int block_q, int block_k, HostPlan* out);
 
 // Picks a block size for T: among the valid sizes (multiples of 16 dividing
-// T, at most 160), the one whose forward key step floor(160 / bk) * bk is
-// longest, the larger on ties.
+// T, at most kStepKeys), the one whose forward key step
+// floor(kStepKeys / bk) * bk is longest, the larger on ties.
 int auto_block(int T);
 
 // ------------------------------------------------------------ prepare
@@ -102,7 +111,8 @@ struct FwdParams {
   int bh;                // batch * heads
   int n;                 // tokens per head
   int bk;                // key block rows
-  int G;                 // blocks per full key step (step keys <= kMaxStepKeys)
+  int G;                 // blocks per full key step (step keys <= kStepKeys)
+  int ns;                // S buffers in tensor memory (2..kMaxSBuf)
   int stages_k, stages_v;
   int force_path;        // -1 auto, 0 fixed, 1 online
   float scale_log2;      // softmax scale * log2(e)

@@ -19,14 +19,14 @@ namespace wsattn {
 
 static bool valid_block(int b, int T) { return b >= 16 && b % 16 == 0 && T % b == 0; }
 
-// The forward kernel streams keys in steps of floor(160 / bk) blocks, so the
-// automatic size is the valid block whose step holds the most keys (ties go
-// to the larger block: fewer TMA boxes per step).
+// The forward kernel streams keys in steps of floor(kStepKeys / bk) blocks,
+// so the automatic size is the valid block whose step holds the most keys;
+// ties go to the larger block (fewer TMA boxes per step).
 int auto_block(int T) {
   int best = 0, best_step = 0;
-  for (int b = 16; b <= kMaxBlockK && b <= T; b += 16) {
+  for (int b = 16; b <= kStepKeys && b <= T; b += 16) {
     if (T % b != 0) continue;
-    const int step = (kMaxStepKeys / b) * b;
+    const int step = (kStepKeys / b) * b;
     if (step >= best_step) {
       best = b;
       best_step = step;
@@ -64,7 +64,7 @@ int build_host_plan(int frames, int tokens_per_frame, int window, int ref_frames
   p.bq = bq; p.bk = bk; p.N = N;
   p.nqb = N / bq;
   p.nkb = N / bk;
-  p.G = bk <= kMaxStepKeys ? kMaxStepKeys / bk : 1;
+  p.G = bk <= kStepKeys ? kStepKeys / bk : 1;
   try {
     // Bitmap and CSR.
     p.bitmap.assign(static_cast<size_t>(p.nqb * p.nkb), 0);

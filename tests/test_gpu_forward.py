@@ -150,6 +150,28 @@ def test_block_sizes_dense_frame_span(bk):
     _full_compare(wl, q, k, v, out)
 
 
+@pytest.mark.parametrize("bk", [48, 64, 96, 192])
+def test_block_sizes_step_buffers(bk):
+    # T = 192: steps of 144 (3 x 48) and 128 (2 x 64) keys with two S
+    # buffers, one 96-key block with three, and 192 (above the kernel's step
+    # limit: rejected)
+    import frame_aligned_window_gb300 as fw
+    wl, q, k, v = micro(43, 1, 2, 128, 5, 1, 192, 1)
+    if bk > 160:
+        plan = fw.wsattn_plan(wl.frames, wl.tokens_per_frame, wl.window, wl.ref_frames,
+                              wl.heads, wl.head_dim, 0, bk)
+        qd, kd, vd = q.cuda(), k.cuda(), v.cuda()
+        fw.wsattn_prepare(plan, qd, kd)
+        with pytest.raises(fw.WsattnError) as e:
+            fw.wsattn_forward(plan, qd, kd, vd)
+        assert e.value.code == 3
+        return
+    _, out, _ = gpu_run(wl, q, k, v, block_k=bk)
+    _full_compare(wl, q, k, v, out)
+    _, online, _ = gpu_run(wl, q, k, v, block_k=bk, force_path=1)
+    _full_compare(wl, q, k, v, online)
+
+
 @pytest.mark.parametrize("case", [
     # seed, B, H, D, F, R, T, w: edge shapes
     (51, 1, 1, 128, 1, 0, 16, 0),      # one frame of 16 tokens (single block, ragged tile)
