@@ -236,8 +236,7 @@ int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, 
   // K and V boxes are one key block; a step of G blocks issues G boxes into
   // consecutive rows of its stage.
   const int step_keys = hp.G * hp.bk;
-  prm.ns = wsattn::forward_s_buffers(hp.D, step_keys);
-  if (prm.ns < 2) return WSATTN_ERR_UNSUPPORTED;
+  if (!wsattn::forward_tmem_fits(hp.D, step_keys)) return WSATTN_ERR_UNSUPPORTED;
   wsattn::forward_stages(hp.D, step_keys, plan->smem_optin, &prm.stages_k, &prm.stages_v);
   prm.force_path = plan->force_path;
   prm.scale_log2 = (1.0f / std::sqrt(static_cast<float>(hp.D))) * 1.4426950408889634f;

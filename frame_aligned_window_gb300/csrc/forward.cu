@@ -26,22 +26,19 @@
 //               (s = 16 * ceil(keys / 32)), so each SMSP runs two softmax warps.
 //
 // Keys are consumed in steps of up to G consecutive active blocks of one run
-// (G * bk <= 160 keys): one TMA box per block lands
-// in consecutive rows of the step's stage (the swizzle pattern continues
-// across boxes), and each MMA covers the whole step.
+// (G * bk <= 160 keys): one TMA box per block lands in consecutive rows of the
+// step's stage (the swizzle pattern continues across boxes), and each MMA
+// covers the whole step.
 //
-// Tensor memory (512 columns): O [0, D), ns S buffers of `step` columns each
-// (two of 160 at D = 128; three or four for shorter steps), then Q (D/2
-// columns of bf16 pairs).  P
-// (keys/2 columns of bf16 pairs) aliases its S buffer from column s/2:
-// warpgroup 0's half lands in columns [s/2, s) and warpgroup 1's in
-// [s, s/2 + keys/2).  Warpgroup 0 walks its 16-column chunks backwards and
-// warpgroup 1 forwards, so every chunk's P lands in S columns its own
-// warpgroup has already read: the two never wait on each other in the
-// fixed-max path, and each holds one chunk (plus the next one in flight) in
-// registers.  The QK^T that refills a buffer waits for the PV that read its
-// P, ns steps back; while the softmax works on S(j) the tensor core runs
-// PV(j-1) and QK^T(j+1 .. j+ns-1).
+// Tensor memory (512 columns at D = 128, 160-key steps): O [0, D), one S
+// buffer (step columns), two P buffers (step/2 columns of bf16 pairs each),
+// Q (D/2 columns of bf16 pairs).  A softmax warp starts a step by loading its
+// S columns into registers and signalling that S is free, so QK^T(j+1)
+// refills S while the softmax of step j computes; P(j) goes to its own
+// buffer (j mod 2), which the PV of step j reads while the softmax already
+// writes P(j+1) to the other one.  The only round trip through the tensor
+// core that the softmax waits on is thus load S(j) -> QK^T(j+1) -> S full,
+// and PV runs beside it.
 //
 // Work items (tile, b*h) go class by class (tiles with equal key lists,
 // longest first) and head by head inside a class, so the CTAs running at one
@@ -76,10 +73,13 @@ enum : int {
   B_OBAR,        // MMA -> softmax: PV(j) done (online path only)
   B_OFULL,       // MMA -> softmax: last PV of the tile done
   B_XCH,         // softmax <-> softmax: row maxima / row sums exchanged
-  B_SFULL0,                       // MMA -> softmax: S buffer i written
-  B_PFULL0 = B_SFULL0 + kMaxSBuf,  // softmax -> MMA: P in S buffer i written
-  B_PVDONE0 = B_PFULL0 + kMaxSBuf, // PV issuer -> QK issuer: PV that read buffer i done
-  B_KFULL0 = B_PVDONE0 + kMaxSBuf,
+  B_SFULL,       // MMA -> softmax: S written (one phase per key step)
+  B_SEMPTY,      // softmax -> MMA: every softmax warp holds its S columns
+  B_PFULL0,      // softmax -> MMA: P buffer 0 / 1 written
+  B_PFULL1,
+  B_PVDONE0,     // MMA -> softmax: the PV that read P buffer 0 / 1 done
+  B_PVDONE1,
+  B_KFULL0,
   B_KEMPTY0 = B_KFULL0 + 4,
   B_VFULL0 = B_KEMPTY0 + 4,
   B_VEMPTY0 = B_VFULL0 + 4,
@@ -147,20 +147,21 @@ __device__ __forceinline__ bool xch_sync(const Shared& s, uint32_t& xc) {
   return ok;
 }
 
-// First S column of warpgroup 1 in a step of `keys` keys; P starts at s/2.
+// First S column of warpgroup 1 in a step of `keys` keys (its P starts at
+// column s/2 of the P buffer).
 __device__ __forceinline__ int split_col(int keys) { return 16 * ((keys / 16 + 1) / 2); }
 
-// Tensor-memory columns: O [0, D), ns S buffers of `step` columns from D,
-// then Q (D/2 columns).
+// Tensor-memory columns: O [0, D), S [D, D + step), P buffers of step/2
+// columns from D + step, Q (D/2 columns) after them.
 struct TmemCols {
-  uint32_t o, s, stride, q;
+  uint32_t o, s, p, pstride, q;
 };
 
 template <int D>
-__device__ __forceinline__ TmemCols tmem_cols(int step_keys, int ns) {
+__device__ __forceinline__ TmemCols tmem_cols(int step_keys) {
   const uint32_t st = static_cast<uint32_t>(step_keys);
-  return TmemCols{0u, static_cast<uint32_t>(D), st,
-                  static_cast<uint32_t>(D) + static_cast<uint32_t>(ns) * st};
+  return TmemCols{0u, static_cast<uint32_t>(D), static_cast<uint32_t>(D) + st, st / 2u,
+                  static_cast<uint32_t>(D) + 2u * st};
 }
 
 struct Item {
@@ -282,9 +283,8 @@ __device__ void producer(const FwdParams& p, const Shared& s) {
 // warp 3 issues O += P V.  A tcgen05.mma blocks its issuing thread while the
 // MMA queue is full, so with one issuer every barrier wait and every bit of
 // bookkeeping between MMA groups left the tensor core idle; with two, one
-// issuer's waits overlap the other's MMAs.  The only hazard between them is
-// the S buffer: QK into buffer b overwrites the P that the previous PV from
-// buffer b reads, so the QK issuer waits on that PV's commit (pv_done[b]).
+// issuer's waits overlap the other's MMAs.  QK^T(j+1) waits only until every
+// softmax warp holds S(j) in registers; PV(j) waits for P(j).
 // Descriptor bases are computed once; each MMA adds a constant to the
 // start-address field (bits 0-13, address >> 4), and the k-step loops are
 // unrolled.
@@ -295,15 +295,16 @@ __device__ void qk_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
   const int ns = G * bk;
   const uint32_t box_pitch = static_cast<uint32_t>(ns) * 128u;
   const uint32_t stage_bytes = box_pitch * kBoxes;
-  const TmemCols tc_ = tmem_cols<D>(ns, p.ns);
+  const TmemCols tc_ = tmem_cols<D>(ns);
   const uint32_t t_s = tbase + tc_.s, t_q = tbase + tc_.q;
   const uint32_t id_qk0 = idesc_bf16_f32(kTileM, 0, false);  // N filled per step
   // K is K-major (SBO 1 KB)
   const uint64_t kdesc0 = sdesc_sw128(s.k, 16, 1024);
   const uint64_t box16 = box_pitch >> 4, stage16 = stage_bytes >> 4;
   const int n_items = p.n_tiles * p.bh;
-  const uint32_t nk = static_cast<uint32_t>(p.stages_k), nsb = static_cast<uint32_t>(p.ns);
-  Ring kr, sr;
+  const uint32_t nk = static_cast<uint32_t>(p.stages_k);
+  Ring kr;
+  uint32_t su = 0;  // parity of the current use of S
   uint32_t tiles_done = 0;
   Steps qs;
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
@@ -313,9 +314,8 @@ __device__ void qk_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
     if (!wait(s, bar(s, B_QTFULL), tiles_done & 1u, kStatusTimeoutMma)) return;
     tc_fence_after();
     for (int j = 0; j < t.nstep; ++j) {
-      // the PV that last read this S buffer (its P) must be done
-      const uint32_t sb = sr.slot;
-      if (!wait(s, bar(s, B_PVDONE0 + sb), sr.phase ^ 1u, kStatusTimeoutMma)) return;
+      // the softmax warps must hold the previous S in registers
+      if (!wait(s, bar(s, B_SEMPTY), su ^ 1u, kStatusTimeoutMma)) return;
       int nb;
       qs.next(G, nb);
       const uint32_t keys = static_cast<uint32_t>(nb * bk);
@@ -323,15 +323,14 @@ __device__ void qk_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
       if (!wait(s, bar(s, B_KFULL0 + slot), kr.phase, kStatusTimeoutMma)) return;
       tc_fence_after();
       const uint64_t kd = kdesc0 + slot * stage16;
-      const uint32_t d_s = t_s + sb * tc_.stride;
       const uint32_t id = id_qk0 | ((keys >> 3) << 17);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        mma_ts(d_s, t_q + kk * 8, kd + (kk / 4) * box16 + (kk % 4) * 2, id, kk > 0 ? 1u : 0u);
+        mma_ts(t_s, t_q + kk * 8, kd + (kk / 4) * box16 + (kk % 4) * 2, id, kk > 0 ? 1u : 0u);
       tc_commit(bar(s, B_KEMPTY0 + slot));
-      tc_commit(bar(s, B_SFULL0 + sb));
+      tc_commit(bar(s, B_SFULL));
       kr.next(nk);
-      sr.next(nsb);
+      su ^= 1u;
     }
     ++tiles_done;
   }
@@ -344,14 +343,14 @@ __device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
   const int ns = G * bk;
   const uint32_t box_pitch = static_cast<uint32_t>(ns) * 128u;
   const uint32_t stage_bytes = box_pitch * kBoxes;
-  const TmemCols tc_ = tmem_cols<D>(ns, p.ns);
-  const uint32_t t_o = tbase + tc_.o, t_s = tbase + tc_.s;
+  const TmemCols tc_ = tmem_cols<D>(ns);
+  const uint32_t t_o = tbase + tc_.o, t_p = tbase + tc_.p;
   const uint32_t id_pv = idesc_bf16_f32(kTileM, D, true);
   // V is MN-major (LBO = the 64-column box pitch)
   const uint64_t vdesc0 = sdesc_sw128(s.v, box_pitch, 1024);
   const uint64_t stage16 = stage_bytes >> 4;
   const int n_items = p.n_tiles * p.bh;
-  const uint32_t nv = static_cast<uint32_t>(p.stages_v), nsb = static_cast<uint32_t>(p.ns);
+  const uint32_t nv = static_cast<uint32_t>(p.stages_v);
   Ring vr, pr;
   Steps ps;
   for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
@@ -365,22 +364,22 @@ __device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
       ps.next(G, nb);
       const int keys = nb * bk;
       const int nks = keys / 16;
-      const uint32_t sb = pr.slot;
-      if (!wait(s, bar(s, B_PFULL0 + sb), pr.phase, kStatusTimeoutMma)) return;
+      const uint32_t pb = pr.slot;
+      if (!wait(s, bar(s, B_PFULL0 + pb), pr.phase, kStatusTimeoutMma)) return;
       const uint32_t vslot = vr.slot;
       if (!wait(s, bar(s, B_VFULL0 + vslot), vr.phase, kStatusTimeoutMma)) return;
       tc_fence_after();
       const uint64_t vd = vdesc0 + vslot * stage16;
-      const uint32_t a_p = t_s + sb * tc_.stride + static_cast<uint32_t>(split_col(keys) / 2);
-      // 16 key rows (2 KB of V) per k-step
+      const uint32_t a_p = t_p + pb * tc_.pstride;
+      // 16 key rows (2 KB of V, 8 P columns) per k-step
       mma_ts(t_o, a_p, vd, id_pv, j > 0 ? 1u : 0u);
 #pragma unroll
       for (int kk = 1; kk < 2 * MAXC; ++kk)
         if (kk < nks) mma_ts(t_o, a_p + kk * 8, vd + kk * 128, id_pv, 1u);
       tc_commit(bar(s, B_VEMPTY0 + vslot));
-      tc_commit(bar(s, B_PVDONE0 + sb));
+      tc_commit(bar(s, B_PVDONE0 + pb));
       vr.next(nv);
-      pr.next(nsb);
+      pr.next(2);
       if (online && j + 1 < nstep) tc_commit(bar(s, B_OBAR));
     }
     tc_commit(bar(s, B_OFULL));
@@ -440,59 +439,27 @@ __device__ __forceinline__ void exp_pack_store(const uint32_t (&sv)[16], uint64_
   tmem_st8(taddr, w);
 }
 
-// Turns this warpgroup's n16 (<= MAXC) chunks of 16 S columns into P, one
-// chunk at a time with the next chunk's TMEM load in flight.  Chunk k sits at
-// S columns sa + 16k and its P at pa + 8k.  Warpgroup 0 (pa = sa + 8 n16)
-// walks its chunks backwards and warpgroup 1 (pa = sa) forwards: either way
-// a chunk's P lands only in S columns already read, so nothing is clobbered
-// before it is loaded.
+// Loads this warpgroup's S columns of the step (MAXC chunks of 16 from sa)
+// into registers with one wait.  Chunks past the step's own (a shorter last
+// step of a run) read neighbouring tensor-memory columns and are ignored.
 template <int MAXC>
-__device__ __forceinline__ void step_exp(uint32_t sa, uint32_t pa, int n16, bool reverse,
-                                         uint64_t c2, uint64_t nb2, uint64_t& la, uint64_t& lb) {
-  uint32_t ra[16], rb[16];
-  auto chunk = [&](int i) { return reverse ? n16 - 1 - i : i; };
-  if (n16 > 0) {
-    tmem_ld16(sa + 16 * chunk(0), ra);
-    tmem_wait_ld16(ra);
-  }
+__device__ __forceinline__ void load_s(uint32_t sa, uint32_t (&sv)[MAXC][16]) {
 #pragma unroll
-  for (int i = 0; i < MAXC; i += 2) {
-    if (i < n16) {
-      if (i + 1 < n16) tmem_ld16(sa + 16 * chunk(i + 1), rb);
-      exp_pack_store(ra, c2, nb2, la, lb, pa + 8 * chunk(i));
-      if (i + 1 < n16) tmem_wait_ld16(rb);
-    }
-    if (i + 1 < n16) {
-      if (i + 2 < n16) tmem_ld16(sa + 16 * chunk(i + 2), ra);
-      exp_pack_store(rb, c2, nb2, la, lb, pa + 8 * chunk(i + 1));
-      if (i + 2 < n16) tmem_wait_ld16(ra);
-    }
-  }
+  for (int c = 0; c < MAXC; ++c) tmem_ld16(sa + 16 * c, sv[c]);
+  tmem_wait_ld();
+#pragma unroll
+  for (int c = 0; c < MAXC; ++c) reg_fence16(sv[c]);
 }
 
-// Steps shorter than a full one (the last step of a run) take the guarded
-// chunk loop out of line, so the fixed-max step loop holds one unrolled,
-// unguarded copy: with the compile-time count the loop is about a quarter
-// faster, and the smaller loop body runs faster again.
-struct Sum2 {
-  uint64_t a, b;
-};
+// p = 2^(s*c + nb) for the first n16 chunks: stores their bf16 pairs at
+// pa + 8c and adds them to the packed row sums.
 template <int MAXC>
-__device__ __noinline__ Sum2 step_exp_short(uint32_t sa, uint32_t pa, int n16, bool reverse,
-                                            uint64_t c2, uint64_t nb2) {
-  Sum2 r{f2_pack(0.f, 0.f), f2_pack(0.f, 0.f)};
-  step_exp<MAXC>(sa, pa, n16, reverse, c2, nb2, r.a, r.b);
-  return r;
-}
-template <int MAXC>
-__device__ __forceinline__ void step_exp_n(uint32_t sa, uint32_t pa, int n16, bool reverse,
-                                           uint64_t c2, uint64_t nb2, uint64_t& la, uint64_t& lb) {
-  if (n16 == MAXC) {
-    step_exp<MAXC>(sa, pa, MAXC, reverse, c2, nb2, la, lb);
-  } else {
-    const Sum2 r = step_exp_short<MAXC>(sa, pa, n16, reverse, c2, nb2);
-    la = f2_add(la, r.a);
-    lb = f2_add(lb, r.b);
+__device__ __forceinline__ void exp_chunks(const uint32_t (&sv)[MAXC][16], int n16, uint64_t c2,
+                                           uint64_t nb2, uint64_t& la, uint64_t& lb,
+                                           uint32_t pa) {
+#pragma unroll
+  for (int c = 0; c < MAXC; ++c) {
+    if (c < n16) exp_pack_store(sv[c], c2, nb2, la, lb, pa + 8 * c);
   }
 }
 
@@ -503,14 +470,14 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
   const int r = (threadIdx.x - kSoftmaxWarp0 * 32) % kTileM;  // tile row == TMEM lane
   const uint32_t lane = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const int bk = p.bk, G = p.G;
-  const TmemCols tc_ = tmem_cols<D>(G * bk, p.ns);
+  const TmemCols tc_ = tmem_cols<D>(G * bk);
   const uint32_t ocol = tc_.o + static_cast<uint32_t>(wg * (D / 2));  // this WG's O half
   const float c = p.scale_log2;
   const uint64_t c2 = f2_pack(c, c);
   const int n_items = p.n_tiles * p.bh;
-  const uint32_t nsb = static_cast<uint32_t>(p.ns);
   uint32_t qc = 0, oc = 0, tiles_done = 0, xpar = 0, xc = 0;
-  Ring sr;
+  uint32_t su = 0;  // parity of the current use of S
+  Ring pr;          // P buffer
 
   int it = blockIdx.x;
   if (it >= n_items) return;
@@ -527,7 +494,8 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
     float m = -INFINITY;
     const float nb_fixed = valid ? -p.m_rows[grow] * kLog2e : 0.f;
     if (!online) {
-      // Fixed max: every step is exp, pack, store; the row sum accumulates.
+      // Fixed max: every step is load, exp, pack, store; the row sum
+      // accumulates.
       const uint64_t nb2 = f2_pack(nb_fixed, nb_fixed);
       uint64_t la = f2_pack(0.f, 0.f), lb = la;
       for (int j = 0; j < t.nstep; ++j) {
@@ -537,16 +505,22 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         const int split = split_col(keys);
         const uint32_t c0 = wg == 0 ? 0u : static_cast<uint32_t>(split);  // first S column
         const int n16 = (wg == 0 ? split : keys - split) / 16;           // 16-column chunks
-        const uint32_t pcol = static_cast<uint32_t>(split / 2) + c0 / 2;  // first P column
-        const uint32_t sb = sr.slot;
-        if (!wait_warp(s, bar(s, B_SFULL0 + sb), sr.phase)) return;
+        if (!wait_warp(s, bar(s, B_SFULL), su)) return;
         tc_fence_after();
-        const uint32_t sbase = lane + tc_.s + sb * tc_.stride;
-        step_exp_n<MAXC>(sbase + c0, sbase + pcol, n16, wg == 0, c2, nb2, la, lb);
+        uint32_t sv[MAXC][16];
+        load_s<MAXC>(lane + tc_.s + c0, sv);
+        tc_fence_before();
+        warp_arrive(bar(s, B_SEMPTY));
+        su ^= 1u;
+        // the PV that read this P buffer two steps back must be done
+        const uint32_t pb = pr.slot;
+        if (!wait_warp(s, bar(s, B_PVDONE0 + pb), pr.phase ^ 1u)) return;
+        tc_fence_after();
+        exp_chunks<MAXC>(sv, n16, c2, nb2, la, lb, lane + tc_.p + pb * tc_.pstride + c0 / 2);
         tmem_wait_st();
         tc_fence_before();
-        warp_arrive(bar(s, B_PFULL0 + sb));
-        sr.next(nsb);
+        warp_arrive(bar(s, B_PFULL0 + pb));
+        pr.next(2);
       }
       const float2 a = f2_unpack(f2_add(la, lb));
       l = a.x + a.y;
@@ -558,19 +532,21 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         const int split = split_col(keys);
         const uint32_t c0 = wg == 0 ? 0u : static_cast<uint32_t>(split);
         const int n16 = (wg == 0 ? split : keys - split) / 16;
-        const uint32_t pcol = static_cast<uint32_t>(split / 2) + c0 / 2;
-        const uint32_t sb = sr.slot;
-        if (!wait_warp(s, bar(s, B_SFULL0 + sb), sr.phase)) return;
+        if (!wait_warp(s, bar(s, B_SFULL), su)) return;
         tc_fence_after();
-        const uint32_t sbase = lane + tc_.s + sb * tc_.stride;
-        // row max of this step over both warpgroups' columns, one chunk at a time
+        uint32_t sv[MAXC][16];
+        load_s<MAXC>(lane + tc_.s + c0, sv);
+        tc_fence_before();
+        warp_arrive(bar(s, B_SEMPTY));
+        su ^= 1u;
+        // row max of this step over both warpgroups' columns
         float mx = -INFINITY;
-        for (int k = 0; k < n16; ++k) {
-          uint32_t ra[16];
-          tmem_ld16(sbase + c0 + 16 * k, ra);
-          tmem_wait_ld16(ra);
 #pragma unroll
-          for (int i = 0; i < 16; ++i) mx = fmaxf(mx, __uint_as_float(ra[i]));
+        for (int k = 0; k < MAXC; ++k) {
+          if (k < n16) {
+#pragma unroll
+            for (int i = 0; i < 16; ++i) mx = fmaxf(mx, __uint_as_float(sv[k][i]));
+          }
         }
         s.xch_m[(xpar * 2 + wg) * kTileM + r] = mx;
         if (!xch_sync(s, xc)) return;
@@ -578,9 +554,12 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         xpar ^= 1u;
         const float m_new = fmaxf(m, fmaxf(mx, mo) * c);
         const float alpha = ex2_approx(m - m_new);
+        const uint32_t pb = pr.slot;
+        if (!wait_warp(s, bar(s, B_PVDONE0 + pb), pr.phase ^ 1u)) return;
+        tc_fence_after();
         uint64_t sa2 = f2_pack(0.f, 0.f), sb2 = sa2;
-        step_exp_n<MAXC>(sbase + c0, sbase + pcol, n16, wg == 0, c2, f2_pack(-m_new, -m_new), sa2,
-                         sb2);
+        exp_chunks<MAXC>(sv, n16, c2, f2_pack(-m_new, -m_new), sa2, sb2,
+                         lane + tc_.p + pb * tc_.pstride + c0 / 2);
         const float2 a = f2_unpack(f2_add(sa2, sb2));
         l = l * alpha + (a.x + a.y);
         m = m_new;
@@ -609,8 +588,8 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         }
         tmem_wait_st();
         tc_fence_before();
-        warp_arrive(bar(s, B_PFULL0 + sb));
-        sr.next(nsb);
+        warp_arrive(bar(s, B_PFULL0 + pb));
+        pr.next(2);
       }
     }
 
@@ -676,8 +655,9 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
     mbar_init(bar(s, B_QTFULL), kSoftmaxWarps);
     mbar_init(bar(s, B_OBAR), 1);
     mbar_init(bar(s, B_OFULL), 1);
-    for (int i = 0; i < kMaxSBuf; ++i) {
-      mbar_init(bar(s, B_SFULL0 + i), 1);
+    mbar_init(bar(s, B_SFULL), 1);
+    mbar_init(bar(s, B_SEMPTY), kSoftmaxWarps);
+    for (int i = 0; i < 2; ++i) {
       mbar_init(bar(s, B_PFULL0 + i), kSoftmaxWarps);
       mbar_init(bar(s, B_PVDONE0 + i), 1);
     }

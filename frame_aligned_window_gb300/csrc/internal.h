@@ -17,15 +17,11 @@ constexpr int kTileM = 128;
 // blocks (one block when bk > 160 is rejected by the forward).
 constexpr int kMaxBlockK = 160;
 constexpr int kStepKeys = 160;
-// Tensor memory (512 columns) holds O (D columns), Q (D/2 columns) and the S
-// buffers the forward rotates through: two of 160 columns at D = 128, three
-// of up to 106, four of up to 80.  The QK^T that refills a buffer waits for
-// the PV that read its P, ns steps back.
+// Tensor memory (512 columns) holds O (D columns), one S buffer (step
+// columns), two P buffers (step/2 columns each) and Q (D/2 columns).
 constexpr int kTmemColumns = 512;
-constexpr int kMaxSBuf = 4;
-inline int forward_s_buffers(int D, int step_keys) {
-  const int n = (kTmemColumns - D - D / 2) / step_keys;
-  return n > kMaxSBuf ? kMaxSBuf : n;
+inline bool forward_tmem_fits(int D, int step_keys) {
+  return D + D / 2 + 2 * step_keys <= kTmemColumns;
 }
 // Default eligibility threshold, in scaled-logit units.
 constexpr float kDefaultTau = 40.0f;
@@ -112,7 +108,6 @@ struct FwdParams {
   int n;                 // tokens per head
   int bk;                // key block rows
   int G;                 // blocks per full key step (step keys <= kStepKeys)
-  int ns;                // S buffers in tensor memory (2..kMaxSBuf)
   int stages_k, stages_v;
   int force_path;        // -1 auto, 0 fixed, 1 online
   float scale_log2;      // softmax scale * log2(e)
