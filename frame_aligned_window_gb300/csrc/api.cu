@@ -218,8 +218,12 @@ int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, 
   const int64_t rows = static_cast<int64_t>(BH) * hp.N;
   FwdParams prm;
   std::memset(&prm, 0, sizeof(prm));
+  // A key step is G consecutive blocks of one run, i.e. G * bk consecutive
+  // rows: K and V are loaded one box of a whole step per 64-column slab.
+  const int step_keys = hp.G * hp.bk;
   if (!encode_map(&prm.tm_q, q, rows, hp.D, wsattn::kTileM) ||
-      !encode_map(&prm.tm_k, k, rows, hp.D, hp.bk) || !encode_map(&prm.tm_v, v, rows, hp.D, hp.bk))
+      !encode_map(&prm.tm_k, k, rows, hp.D, step_keys) ||
+      !encode_map(&prm.tm_v, v, rows, hp.D, step_keys))
     return WSATTN_ERR_CUDA;
   prm.tiles = plan->d_tiles;
   prm.cls = plan->d_cls;
@@ -233,9 +237,6 @@ int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, 
   prm.n = static_cast<int>(hp.N);
   prm.bk = hp.bk;
   prm.G = hp.G;
-  // K and V boxes are one key block; a step of G blocks issues G boxes into
-  // consecutive rows of its stage.
-  const int step_keys = hp.G * hp.bk;
   if (!wsattn::forward_tmem_fits(hp.D, step_keys)) return WSATTN_ERR_UNSUPPORTED;
   wsattn::forward_stages(hp.D, step_keys, plan->smem_optin, &prm.stages_k, &prm.stages_v);
   prm.force_path = plan->force_path;

@@ -26,9 +26,8 @@
 //               (s = 16 * ceil(keys / 32)), so each SMSP runs two softmax warps.
 //
 // Keys are consumed in steps of up to G consecutive active blocks of one run
-// (G * bk <= 160 keys): one TMA box per block lands in consecutive rows of the
-// step's stage (the swizzle pattern continues across boxes), and each MMA
-// covers the whole step.
+// (G * bk <= 160 keys): the step's rows are consecutive, so K and V arrive as
+// one TMA box per 64-column slab, and each MMA covers the whole step.
 //
 // Tensor memory (512 columns at D = 128, 160-key steps): O [0, D), one S
 // buffer (step columns), two P buffers (step/2 columns of bf16 pairs each),
@@ -216,15 +215,16 @@ struct Steps {
 };
 
 // ------------------------------------------------------------------ producer
+// A step's G blocks are consecutive rows of one run, so each step is one TMA
+// box per 64-column slab (G * bk rows).  The shorter last step of a run
+// loads the whole box too: the rows past it are never read by an MMA.
 template <int D>
 __device__ void producer(const FwdParams& p, const Shared& s) {
   constexpr int kBoxes = D / 64;
   const int bk = p.bk, G = p.G;
-  const uint32_t ns = static_cast<uint32_t>(G * bk);     // rows of a full step
+  const uint32_t ns = static_cast<uint32_t>(G * bk);     // rows of a step
   const uint32_t box_pitch = ns * 128u;                  // a 64-column box of a stage
   const uint32_t stage_bytes = box_pitch * kBoxes;
-  const uint32_t blk_rows_bytes = static_cast<uint32_t>(bk) * 128u;
-  const uint32_t blk_tx = static_cast<uint32_t>(bk) * D * 2u;
   const int n_items = p.n_tiles * p.bh;
   const uint32_t nk = static_cast<uint32_t>(p.stages_k), nv = static_cast<uint32_t>(p.stages_v);
   Ring kr, vr;
@@ -246,32 +246,24 @@ __device__ void producer(const FwdParams& p, const Shared& s) {
     for (int j = 0; j <= t.nstep; ++j) {
       if (j < t.nstep) {
         int nb;
-        const int first = ks.next(G, nb);
+        const int row = y0 + ks.next(G, nb) * bk;
         if (!wait(s, bar(s, B_KEMPTY0 + kr.slot), kr.phase ^ 1u, kStatusTimeoutProducer)) return;
         const uint32_t fb = bar(s, B_KFULL0 + kr.slot);
-        mbar_arrive_expect_tx(fb, blk_tx * nb);
+        mbar_arrive_expect_tx(fb, stage_bytes);
         const uint32_t dst = s.k + kr.slot * stage_bytes;
-        for (int b = 0; b < nb; ++b) {
-          const int row = y0 + (first + b) * bk;
 #pragma unroll
-          for (int c = 0; c < kBoxes; ++c)
-            tma_load_2d(dst + c * box_pitch + b * blk_rows_bytes, &p.tm_k, fb, c * 64, row);
-        }
+        for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_k, fb, c * 64, row);
         kr.next(nk);
       }
       if (j >= 1) {
         int nb;
-        const int first = vs.next(G, nb);
+        const int row = y0 + vs.next(G, nb) * bk;
         if (!wait(s, bar(s, B_VEMPTY0 + vr.slot), vr.phase ^ 1u, kStatusTimeoutProducer)) return;
         const uint32_t fb = bar(s, B_VFULL0 + vr.slot);
-        mbar_arrive_expect_tx(fb, blk_tx * nb);
+        mbar_arrive_expect_tx(fb, stage_bytes);
         const uint32_t dst = s.v + vr.slot * stage_bytes;
-        for (int b = 0; b < nb; ++b) {
-          const int row = y0 + (first + b) * bk;
 #pragma unroll
-          for (int c = 0; c < kBoxes; ++c)
-            tma_load_2d(dst + c * box_pitch + b * blk_rows_bytes, &p.tm_v, fb, c * 64, row);
-        }
+        for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_v, fb, c * 64, row);
         vr.next(nv);
       }
     }

@@ -94,8 +94,8 @@ void prepare_chunking(int BH, int64_t N, int num_sms, int* nchunk, int* rows_per
 // ------------------------------------------------------------ forward
 struct FwdParams {
   CUtensorMap tm_q;  // [BH*N, D] bf16, box {64, 128}, 128-byte swizzle
-  CUtensorMap tm_k;  // [BH*N, D] bf16, box {64, bk}
-  CUtensorMap tm_v;  // [BH*N, D] bf16, box {64, bk}
+  CUtensorMap tm_k;  // [BH*N, D] bf16, box {64, G * bk}
+  CUtensorMap tm_v;  // [BH*N, D] bf16, box {64, G * bk}
   const WorkTile* tiles;
   const int32_t* cls;    // class boundaries into tiles, n_cls + 1 entries
   int n_cls;
