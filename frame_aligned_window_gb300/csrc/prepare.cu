@@ -34,6 +34,9 @@ namespace wsattn {
 namespace {
 
 constexpr int kPrepThreads = 256;
+// Rows a thread group loads before it reduces any of them: the passes are
+// bound by HBM only with several 16-byte loads in flight per thread.
+constexpr int kUnroll = 4;
 
 // Eight bf16 in a 16-byte word -> fp32 (exact: bf16 is the top half of fp32).
 __device__ __forceinline__ void unpack8(const uint4& u, float (&f)[8]) {
@@ -78,12 +81,21 @@ __global__ void __launch_bounds__(kPrepThreads)
   const int64_t r1 = min(n, r0 + rpc);
   const size_t base = static_cast<size_t>(bh) * n;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  for (int64_t r = r0 + rs; r < r1; r += kRows) {
-    const uint4 kv = __ldg(reinterpret_cast<const uint4*>(k + (base + r) * D) + lr);
-    float kf[8];
-    unpack8(kv, kf);
+  for (int64_t rb = r0; rb < r1; rb += kRows * kUnroll) {
+    uint4 kv[kUnroll];
 #pragma unroll
-    for (int i = 0; i < 8; ++i) acc[i] += kf[i];
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t r = rb + u * kRows + rs;
+      kv[u] = r < r1 ? __ldg(reinterpret_cast<const uint4*>(k + (base + r) * D) + lr)
+                     : make_uint4(0u, 0u, 0u, 0u);
+    }
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      float kf[8];
+      unpack8(kv[u], kf);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] += kf[i];
+    }
   }
 #pragma unroll
   for (int i = 0; i < 8; ++i) red[rs][lr * 8 + i] = acc[i];
@@ -123,33 +135,48 @@ __global__ void __launch_bounds__(kPrepThreads)
   const int64_t r1 = min(n, r0 + rpc);
   const size_t base = static_cast<size_t>(bh) * n;
   float km = 0.f, qm = 0.f;
-  for (int64_t rb = r0; rb < r1; rb += kRows) {  // uniform trip count per warp
-    const int64_t r = rb + rs;
-    float kss = 0.f, qss = 0.f, qmu = 0.f;
-    if (r < r1) {
-      const uint4 kv = __ldg(reinterpret_cast<const uint4*>(k + (base + r) * D) + lr);
-      const uint4 qv = __ldg(reinterpret_cast<const uint4*>(q + (base + r) * D) + lr);
-      float kf[8], qf[8];
-      unpack8(kv, kf);
-      unpack8(qv, qf);
+  for (int64_t rb = r0; rb < r1; rb += kRows * kUnroll) {  // uniform trip count per warp
+    uint4 kv[kUnroll], qv[kUnroll];
 #pragma unroll
-      for (int i = 0; i < 8; ++i) {
-        const float x = kf[i] - mloc[i];
-        kss = fmaf(x, x, kss);
-        qss = fmaf(qf[i], qf[i], qss);
-        qmu = fmaf(qf[i], mloc[i], qmu);
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t r = rb + u * kRows + rs;
+      if (r < r1) {
+        kv[u] = __ldg(reinterpret_cast<const uint4*>(k + (base + r) * D) + lr);
+        qv[u] = __ldg(reinterpret_cast<const uint4*>(q + (base + r) * D) + lr);
+      } else {
+        kv[u] = make_uint4(0u, 0u, 0u, 0u);
+        qv[u] = kv[u];
       }
     }
-    kss = group_sum<kLanes>(kss);
-    qss = group_sum<kLanes>(qss);
-    qmu = group_sum<kLanes>(qmu);
-    const float qnorm = sqrtf(qss);
-    if (r < r1 && lr == 0) {
-      qn[base + r] = qnorm;
-      crow[base + r] = scale * qmu;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      const int64_t r = rb + u * kRows + rs;
+      float kss = 0.f, qss = 0.f, qmu = 0.f;
+      if (r < r1) {
+        float kf[8], qf[8];
+        unpack8(kv[u], kf);
+        unpack8(qv[u], qf);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) {
+          const float x = kf[i] - mloc[i];
+          kss = fmaf(x, x, kss);
+          qss = fmaf(qf[i], qf[i], qss);
+          qmu = fmaf(qf[i], mloc[i], qmu);
+        }
+      }
+      kss = group_sum<kLanes>(kss);
+      qss = group_sum<kLanes>(qss);
+      qmu = group_sum<kLanes>(qmu);
+      const float qnorm = sqrtf(qss);
+      if (r < r1 && lr == 0) {
+        qn[base + r] = qnorm;
+        crow[base + r] = scale * qmu;
+      }
+      if (r < r1) {
+        km = fmaxf(km, sqrtf(kss));
+        qm = fmaxf(qm, qnorm);
+      }
     }
-    km = fmaxf(km, sqrtf(kss));
-    qm = fmaxf(qm, qnorm);
   }
   const float kmb = block_max(km, wmax);
   __syncthreads();  // wmax is reused
