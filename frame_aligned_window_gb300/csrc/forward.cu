@@ -306,13 +306,15 @@ __device__ void qk_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
     if (!wait(s, bar(s, B_QTFULL), tiles_done & 1u, kStatusTimeoutMma)) return;
     tc_fence_after();
     for (int j = 0; j < t.nstep; ++j) {
-      // the softmax warps must hold the previous S in registers
-      if (!wait(s, bar(s, B_SEMPTY), su ^ 1u, kStatusTimeoutMma)) return;
       int nb;
       qs.next(G, nb);
       const uint32_t keys = static_cast<uint32_t>(nb * bk);
       const uint32_t slot = kr.slot;
+      // K is normally resident long before S is free: wait for it first, so
+      // the wait that gates the MMAs is the softmax's.
       if (!wait(s, bar(s, B_KFULL0 + slot), kr.phase, kStatusTimeoutMma)) return;
+      // the softmax warps must hold the previous S in registers
+      if (!wait(s, bar(s, B_SEMPTY), su ^ 1u, kStatusTimeoutMma)) return;
       tc_fence_after();
       const uint64_t kd = kdesc0 + slot * stage16;
       const uint32_t id = id_qk0 | ((keys >> 3) << 17);
