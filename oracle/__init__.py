@@ -60,6 +60,8 @@ def _load():
             lib.orc_blockmap.argtypes = [L, L, L, L, L, L, P, P, P, L, P]
             lib.orc_blockmap.restype = ctypes.c_int
             lib.orc_prepare.argtypes = [P, P, L, L, L, D, D, P, P, P, P, P, P]
+            lib.orc_prepare_window.argtypes = [P, P, L, L, L, L, L, L, L, D, D, P, P, P, P,
+                                               P, P]
             lib.orc_attention_rows.argtypes = [P, P, P, L, L, L, L, L, L, D, L, P, P, P]
             lib.orc_attention_rows_fixed.argtypes = [P, P, P, P, P, L, L, L, L, L, L, D, L,
                                                      P, P, P]
@@ -125,6 +127,18 @@ def prepare(q, k, scale: float, tau: float = TAU) -> dict:
     b = np.zeros((nbh, n)); bmax = np.zeros(nbh); elig = np.zeros(nbh, dtype=np.uint8)
     _load().orc_prepare(_ptr(qd), _ptr(kd), nbh, n, d, scale, tau, _ptr(mu), _ptr(kmax),
                         _ptr(qn), _ptr(b), _ptr(bmax), _ptr(elig))
+    return {"mu": mu, "kmax": kmax, "qn": qn, "b": b, "bmax": bmax, "elig": elig}
+
+
+def prepare_window(q, k, F, T, w, R, scale: float, tau: float = TAU) -> dict:
+    """Like prepare(), with each row's bound over the keys its row attends
+    (the mask walked element by element).  kmax stays the global maximum."""
+    qd, kd = as_f64(q), as_f64(k)
+    nbh, n, d = kd.shape
+    mu = np.zeros((nbh, d)); kmax = np.zeros(nbh); qn = np.zeros((nbh, n))
+    b = np.zeros((nbh, n)); bmax = np.zeros(nbh); elig = np.zeros(nbh, dtype=np.uint8)
+    _load().orc_prepare_window(_ptr(qd), _ptr(kd), nbh, n, d, F, T, w, R, scale, tau, _ptr(mu),
+                               _ptr(kmax), _ptr(qn), _ptr(b), _ptr(bmax), _ptr(elig))
     return {"mu": mu, "kmax": kmax, "qn": qn, "b": b, "bmax": bmax, "elig": elig}
 
 

@@ -20,6 +20,8 @@
  *                       (query norm times the max key norm), per-head
  *                       eligibility (a bound far above the true max makes the
  *                       exponentials underflow).
+ *   orc_prepare_window  the same with each row's bound over the keys it
+ *                       attends (the window, not all keys).
  *   orc_attention_rows  the plain definition: masked softmax(q k^T * scale) v
  *                       over the element-by-element mask, max-subtracted.
  *   orc_attention_rows_fixed   Fig. 4 bottom: the row bound as a fixed max.
@@ -160,6 +162,59 @@ void orc_prepare(const double* q, const double* k, long nbh, long n, long d, dou
     bmax[h] = bm;
     elig[h] = (uint8_t)((bm <= tau) && rows_ok);
   }
+}
+
+/* The same statistics with the window bound (the tighter variant of the
+ * section "Breaking softmax's dependency chain": any key set that contains a
+ * row's active keys bounds its logits, and the smallest is the row's own):
+ *   mu, kmax, qn  as in orc_prepare (kmax stays the global maximum);
+ *   b[h][i]  = scale * qn[h][i] * max_{j : M[i, j] = 1} || k_j - mu ||
+ *              (the mask walked element by element for every row);
+ *   bmax, elig    from these b as in orc_prepare. */
+void orc_prepare_window(const double* q, const double* k, long nbh, long n, long d, long F,
+                        long T, long w, long R, double scale, double tau, double* mu,
+                        double* kmax, double* qn, double* b, double* bmax, uint8_t* elig) {
+  const double underflow_limit = 126.0 * log(2.0);
+  double* knorm = (double*)malloc(sizeof(double) * (size_t)n * (size_t)nbh);
+  if (!knorm) return;
+#pragma omp parallel for schedule(dynamic, 1)
+  for (long h = 0; h < nbh; ++h) {
+    const double* kh = k + h * n * d;
+    const double* qh = q + h * n * d;
+    double* m = mu + h * d;
+    double* kn = knorm + h * n;
+    for (long c = 0; c < d; ++c) m[c] = 0.0;
+    for (long j = 0; j < n; ++j)
+      for (long c = 0; c < d; ++c) m[c] += kh[j * d + c];
+    for (long c = 0; c < d; ++c) m[c] /= (double)n;
+    double km = 0.0;
+    for (long j = 0; j < n; ++j) {
+      double s = 0.0;
+      for (long c = 0; c < d; ++c) {
+        double x = kh[j * d + c] - m[c];
+        s += x * x;
+      }
+      kn[j] = sqrt(s);
+      if (kn[j] > km) km = kn[j];
+    }
+    kmax[h] = km;
+    double bm = 0.0;
+    int rows_ok = 1;
+    for (long i = 0; i < n; ++i) {
+      double s = 0.0;
+      for (long c = 0; c < d; ++c) s += qh[i * d + c] * qh[i * d + c];
+      qn[h * n + i] = sqrt(s);
+      double kw = 0.0;
+      for (long j = 0; j < n; ++j)
+        if (orc_mask(F, T, w, R, i, j) && kn[j] > kw) kw = kn[j];
+      b[h * n + i] = scale * qn[h * n + i] * kw;
+      if (b[h * n + i] > bm) bm = b[h * n + i];
+      if (!(2.0 * b[h * n + i] < underflow_limit)) rows_ok = 0;
+    }
+    bmax[h] = bm;
+    elig[h] = (uint8_t)((bm <= tau) && rows_ok);
+  }
+  free(knorm);
 }
 
 /* Scratch of N doubles per thread for the logits of one row. */
