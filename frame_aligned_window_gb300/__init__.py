@@ -9,8 +9,8 @@ package raises: there is no fallback implementation.
 The names mirror the C ABI:
     wsattn_plan, wsattn_plan_destroy, wsattn_prepare, wsattn_forward,
     wsattn_plan_info, wsattn_get_block_map, wsattn_get_csr, wsattn_get_stats,
-    wsattn_plan_set_debug, wsattn_device_status, wsattn_selftest_timeout,
-    wsattn_status_string, wsattn_prepare_static
+    wsattn_plan_set_debug, wsattn_plan_set_bound, wsattn_device_status,
+    wsattn_selftest_timeout, wsattn_status_string, wsattn_prepare_static
 """
 from __future__ import annotations
 
@@ -26,9 +26,13 @@ LIB_PATH = os.path.join(_HERE, "libwsattn.so")
 EXPORTS = (
     "wsattn_plan", "wsattn_plan_destroy", "wsattn_prepare", "wsattn_forward",
     "wsattn_plan_info", "wsattn_get_block_map", "wsattn_get_csr", "wsattn_get_stats",
-    "wsattn_plan_set_debug", "wsattn_device_status", "wsattn_selftest_timeout",
-    "wsattn_status_string", "wsattn_prepare_static",
+    "wsattn_plan_set_debug", "wsattn_plan_set_bound", "wsattn_device_status",
+    "wsattn_selftest_timeout", "wsattn_status_string", "wsattn_prepare_static",
 )
+
+# wsattn_bound
+BOUND_GLOBAL = 0
+BOUND_WINDOW = 1
 
 STATUS = {0: "OK", 1: "BAD_ARG", 2: "BAD_BLOCK", 3: "UNSUPPORTED", 4: "NOT_PREPARED",
           5: "BATCH_MISMATCH", 6: "CUDA", 7: "TIMEOUT", 8: "NO_MEMORY"}
@@ -55,6 +59,7 @@ _lib.wsattn_get_block_map.argtypes = [_P, _P, _SZ]
 _lib.wsattn_get_csr.argtypes = [_P, _P, _P, _SZ, _SZ]
 _lib.wsattn_get_stats.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P]
 _lib.wsattn_plan_set_debug.argtypes = [_P, _I, _F]
+_lib.wsattn_plan_set_bound.argtypes = [_P, _I]
 _lib.wsattn_device_status.argtypes = [_P, _P]
 _lib.wsattn_selftest_timeout.argtypes = [_I, ctypes.POINTER(_I), _P]
 _lib.wsattn_status_string.argtypes = [_I]
@@ -212,6 +217,12 @@ def wsattn_get_stats(plan: Plan, batch: int, stream=None) -> dict:
 def wsattn_plan_set_debug(plan: Plan, force_path: int = -1, tau: float = 0.0):
     _check(_lib.wsattn_plan_set_debug(plan.handle, int(force_path), float(tau)),
            "wsattn_plan_set_debug")
+
+
+def wsattn_plan_set_bound(plan: Plan, mode: int):
+    """BOUND_GLOBAL (default) or BOUND_WINDOW: the key-norm maximum of the row
+    bounds; prepare again before the next forward."""
+    _check(_lib.wsattn_plan_set_bound(plan.handle, int(mode)), "wsattn_plan_set_bound")
 
 
 def wsattn_device_status(plan: Plan, stream=None) -> int:

@@ -31,6 +31,7 @@ struct wsattn_plan_s {
   int prepared_batch = 0;
   int force_path = -1;
   float tau = wsattn::kDefaultTau;
+  int bound_mode = WSATTN_BOUND_GLOBAL;
 };
 
 namespace {
@@ -106,6 +107,9 @@ int ensure_workspace(wsattn_plan_s* p, int batch, cudaStream_t stream) {
   size_t slots = static_cast<size_t>(BH) * nchunk;
   const size_t bound = static_cast<size_t>(4) * p->num_sms + BH;
   if (slots < bound) slots = bound;
+  // window bounds use one chunk per frame
+  const size_t frame_slots = static_cast<size_t>(BH) * (hp.F + hp.R);
+  if (slots < frame_slots) slots = frame_slots;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t n_b = up(sizeof(float) * BH * hp.N);  // b_rows, and again for m_rows
   const size_t n_mu = up(sizeof(float) * BH * hp.D);
@@ -191,12 +195,20 @@ int wsattn_prepare(wsattn_plan_t plan, int batch, const void* q, const void* k, 
   if (rc != WSATTN_OK) return rc;
   const int BH = batch * hp.H;
   int nchunk = 0, rpc = 0;
-  wsattn::prepare_chunking(BH, hp.N, plan->num_sms, &nchunk, &rpc);
+  wsattn::FrameWindow win{hp.F + hp.R, hp.R, hp.w};
+  const bool window = plan->bound_mode == WSATTN_BOUND_WINDOW;
+  if (window) {
+    nchunk = win.nf;  // one chunk per frame: its maxima are the frame's
+    rpc = hp.T;
+  } else {
+    wsattn::prepare_chunking(BH, hp.N, plan->num_sms, &nchunk, &rpc);
+  }
   PrepBuffers b = plan->buf;
   b.nchunk = nchunk;
   b.rows_per_chunk = rpc;
   const float scale = 1.0f / std::sqrt(static_cast<float>(hp.D));
-  if (wsattn::launch_prepare(q, k, BH, hp.N, hp.D, scale, plan->tau, b, s) != cudaSuccess)
+  if (wsattn::launch_prepare(q, k, BH, hp.N, hp.D, scale, plan->tau, b, window ? &win : nullptr,
+                             s) != cudaSuccess)
     return WSATTN_ERR_CUDA;
   plan->prepared_batch = batch;
   return WSATTN_OK;
@@ -315,6 +327,14 @@ int wsattn_plan_set_debug(wsattn_plan_t plan, int force_path, float tau) {
   if (!plan || force_path < -1 || force_path > 1 || !(tau >= 0.0f)) return WSATTN_ERR_BAD_ARG;
   plan->force_path = force_path;
   if (tau > 0.0f) plan->tau = tau;
+  return WSATTN_OK;
+}
+
+int wsattn_plan_set_bound(wsattn_plan_t plan, int mode) {
+  if (!plan || (mode != WSATTN_BOUND_GLOBAL && mode != WSATTN_BOUND_WINDOW))
+    return WSATTN_ERR_BAD_ARG;
+  plan->bound_mode = mode;
+  plan->prepared_batch = 0;  // the statistics depend on the mode
   return WSATTN_OK;
 }
 

@@ -84,9 +84,20 @@ struct PrepBuffers {
   int rows_per_chunk;
 };
 
-// Enqueues the three prepare passes; returns a cudaError_t.
+// Frame structure for window bounds: chunk c of a head is frame c (T rows),
+// and query frame a attends key frame g iff g < R, a < R or |a - g| <= w.
+struct FrameWindow {
+  int nf;  // R + F frames (= chunks per head)
+  int R;
+  int w;
+};
+
+// Enqueues the three prepare passes; returns a cudaError_t.  With `win`
+// non-null the chunks must be the frames and the row bounds use the
+// per-window key-norm maximum.
 cudaError_t launch_prepare(const void* q, const void* k, int BH, int64_t N, int D, float scale,
-                           float tau, const PrepBuffers& buf, cudaStream_t stream);
+                           float tau, const PrepBuffers& buf, const FrameWindow* win,
+                           cudaStream_t stream);
 
 // Chunking of the N rows of one head across CTAs.
 void prepare_chunking(int BH, int64_t N, int num_sms, int* nchunk, int* rows_per_chunk);

@@ -22,7 +22,9 @@
 //   B  mu = ordered sum of the chunk sums / N; key norms ||k_j - mu|| and
 //      their per-chunk max; query norms ||q_i||, c_i, per-chunk max query
 //      norm (row norms reduced with warp shuffles)        (reads k and q)
-//   C  K_h = max of the chunk maxima; b_i = (scale ||q_i||) K_h;
+//   C  K_h = max of the chunk maxima (with window bounds, where the chunks
+//      are the frames: the max over the frames the row's frame attends);
+//      b_i = (scale ||q_i||) K_h;
 //      m_i = b_i + c_i; B_h = (scale max ||q_i||) K_h, which equals max_i b_i
 //      because the expression is monotone in ||q_i||;
 //      eligible = B_h <= tau and 2 B_h < 126 ln 2.
@@ -222,6 +224,51 @@ __global__ void __launch_bounds__(kPrepThreads)
   }
 }
 
+// Window bounds (one chunk per frame): K_a = largest per-frame key-norm
+// maximum over the frames query frame a attends; b_i = (scale ||q_i||) K_a;
+// B_h = max_a (scale max_{i in a} ||q_i||) K_a, which equals max_i b_i (the
+// expression is monotone in ||q_i||).  kmax keeps the head's global maximum.
+__global__ void __launch_bounds__(kPrepThreads)
+    prep_pass_c_window(int64_t n, int rpc, int nchunk, int R, int w, float scale, float tau,
+                       float* __restrict__ b_rows, float* __restrict__ m_rows,
+                       const float* __restrict__ part_kmax, const float* __restrict__ part_qmax,
+                       float* __restrict__ kmax, float* __restrict__ bmax,
+                       uint8_t* __restrict__ elig) {
+  __shared__ float k_s;
+  const int bh = blockIdx.y, a = blockIdx.x;
+  const float* pk = part_kmax + static_cast<size_t>(bh) * nchunk;
+  auto window_max = [&](int f) {
+    float kh = 0.f;
+    for (int g = 0; g < nchunk; ++g) {
+      const int d = f > g ? f - g : g - f;
+      if (g < R || f < R || d <= w) kh = fmaxf(kh, pk[g]);
+    }
+    return kh;
+  };
+  if (threadIdx.x == 0) k_s = window_max(a);
+  __syncthreads();
+  const float kh = k_s;
+  const int64_t r0 = static_cast<int64_t>(a) * rpc;
+  const int64_t r1 = min(n, r0 + rpc);
+  const size_t base = static_cast<size_t>(bh) * n;
+  for (int64_t r = r0 + threadIdx.x; r < r1; r += kPrepThreads) {
+    const float b = (scale * b_rows[base + r]) * kh;  // b_rows holds ||q_i|| here
+    b_rows[base + r] = b;
+    m_rows[base + r] = b + m_rows[base + r];          // m_rows holds c_i here
+  }
+  if (a == 0 && threadIdx.x == 0) {
+    float kg = 0.f, bm = 0.f;
+    for (int f = 0; f < nchunk; ++f) {
+      kg = fmaxf(kg, pk[f]);
+      bm = fmaxf(bm, (scale * part_qmax[static_cast<size_t>(bh) * nchunk + f]) * window_max(f));
+    }
+    const float underflow_limit = 126.0f * 0.693147180559945309f;
+    kmax[bh] = kg;
+    bmax[bh] = bm;
+    elig[bh] = static_cast<uint8_t>(bm <= tau && 2.0f * bm < underflow_limit);
+  }
+}
+
 }  // namespace
 
 void prepare_chunking(int BH, int64_t N, int num_sms, int* nchunk, int* rows_per_chunk) {
@@ -237,7 +284,8 @@ void prepare_chunking(int BH, int64_t N, int num_sms, int* nchunk, int* rows_per
 }
 
 cudaError_t launch_prepare(const void* q, const void* k, int BH, int64_t N, int D, float scale,
-                           float tau, const PrepBuffers& b, cudaStream_t stream) {
+                           float tau, const PrepBuffers& b, const FrameWindow* win,
+                           cudaStream_t stream) {
   const dim3 grid(b.nchunk, BH);
   const uint16_t* q16 = static_cast<const uint16_t*>(q);
   const uint16_t* k16 = static_cast<const uint16_t*>(k);
@@ -254,9 +302,14 @@ cudaError_t launch_prepare(const void* q, const void* k, int BH, int64_t N, int 
         q16, k16, N, b.rows_per_chunk, b.nchunk, scale, b.part_sum, b.mu, b.b_rows, b.m_rows,
         b.part_kmax, b.part_qmax);
   }
-  prep_pass_c<<<grid, kPrepThreads, 0, stream>>>(N, b.rows_per_chunk, b.nchunk, scale, tau,
-                                                 b.b_rows, b.m_rows, b.part_kmax, b.part_qmax,
-                                                 b.kmax, b.bmax, b.elig);
+  if (win)
+    prep_pass_c_window<<<grid, kPrepThreads, 0, stream>>>(
+        N, b.rows_per_chunk, b.nchunk, win->R, win->w, scale, tau, b.b_rows, b.m_rows,
+        b.part_kmax, b.part_qmax, b.kmax, b.bmax, b.elig);
+  else
+    prep_pass_c<<<grid, kPrepThreads, 0, stream>>>(N, b.rows_per_chunk, b.nchunk, scale, tau,
+                                                   b.b_rows, b.m_rows, b.part_kmax, b.part_qmax,
+                                                   b.kmax, b.bmax, b.elig);
   return cudaGetLastError();
 }
 

@@ -192,6 +192,32 @@ int wsattn_get_stats(wsattn_plan_t plan, float* b_rows, float* m_rows, float* mu
  * eligibility threshold used by later prepares (40 by default). */
 int wsattn_plan_set_debug(wsattn_plan_t plan, int force_path, float tau);
 
+/* Key-norm maximum the row bounds use (see wsattn_plan_set_bound). */
+enum wsattn_bound {
+  WSATTN_BOUND_GLOBAL = 0, /* K_h = max over all N centered keys of the head (default) */
+  WSATTN_BOUND_WINDOW = 1  /* K_h,a = max over the keys frame a attends */
+};
+
+/*
+ * Selects the key-norm maximum of the row bounds for later prepares.  The
+ * bound of the section "Breaking softmax's dependency chain" multiplies a
+ * query's norm by the largest centered key norm; any key subset that
+ * contains the row's active keys gives a valid bound, and the smallest one
+ * is the row's own window:
+ *   WSATTN_BOUND_GLOBAL  b_i = scale * ||q_i|| * max_j ||k_j - mu||  (all N keys)
+ *   WSATTN_BOUND_WINDOW  b_i = scale * ||q_i|| * max_{j attended by i} ||k_j - mu||
+ * Every query of a frame attends the same keys, so the window maximum is one
+ * value per (b, h, query frame): the largest per-frame maximum over the
+ * frames it attends.  m_i, B_h and eligibility follow from b_i as described
+ * at wsattn_prepare; the window bound is never larger, so B_h can only fall
+ * and heads can only become eligible.  Outputs are unchanged in exact
+ * arithmetic.  In window mode wsattn_get_stats' kmax still reports the
+ * global maximum of each head.  The plan must be prepared again before the
+ * next forward.
+ * Errors: BAD_ARG (unknown mode).
+ */
+int wsattn_plan_set_bound(wsattn_plan_t plan, int mode);
+
 /* Synchronises `stream` and reports the plan's device status word: OK, or
  * TIMEOUT if a device-side wait of a kernel launched with this plan expired
  * (the word is then cleared).  CUDA if the synchronisation itself failed. */
