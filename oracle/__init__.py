@@ -54,18 +54,18 @@ def _load():
         if _lib is None:
             lib = ctypes.CDLL(build())
             L, P, D = ctypes.c_long, ctypes.c_void_p, ctypes.c_double
-            lib.orc_mask.argtypes = [L, L, L, L, L, L]
+            lib.orc_mask.argtypes = [L, L, L, L, L, L, L]
             lib.orc_mask.restype = ctypes.c_int
-            lib.orc_mask_dense.argtypes = [L, L, L, L, P]
-            lib.orc_blockmap.argtypes = [L, L, L, L, L, L, P, P, P, L, P]
+            lib.orc_mask_dense.argtypes = [L, L, L, L, L, P]
+            lib.orc_blockmap.argtypes = [L, L, L, L, L, L, L, P, P, P, L, P]
             lib.orc_blockmap.restype = ctypes.c_int
             lib.orc_prepare.argtypes = [P, P, L, L, L, D, D, P, P, P, P, P, P]
-            lib.orc_prepare_window.argtypes = [P, P, L, L, L, L, L, L, L, D, D, P, P, P, P,
-                                               P, P]
-            lib.orc_attention_rows.argtypes = [P, P, P, L, L, L, L, L, L, D, L, P, P, P]
-            lib.orc_attention_rows_fixed.argtypes = [P, P, P, P, P, L, L, L, L, L, L, D, L,
+            lib.orc_prepare_window.argtypes = [P, P, L, L, L, L, L, L, L, L, D, D, P, P, P,
+                                               P, P, P]
+            lib.orc_attention_rows.argtypes = [P, P, P, L, L, L, L, L, L, L, D, L, P, P, P]
+            lib.orc_attention_rows_fixed.argtypes = [P, P, P, P, P, L, L, L, L, L, L, L, D, L,
                                                      P, P, P]
-            lib.orc_attention_rows_online.argtypes = [P, P, P, L, L, L, L, L, L, D, L, L, P,
+            lib.orc_attention_rows_online.argtypes = [P, P, P, L, L, L, L, L, L, L, D, L, L, P,
                                                       P, P]
             lib.orc_num_threads.restype = ctypes.c_int
             _lib = lib
@@ -89,18 +89,25 @@ def as_f64(x) -> np.ndarray:
     return x.reshape(-1, x.shape[-2], x.shape[-1])
 
 
-def mask(F, T, w, R, i, j) -> int:
-    return int(_load().orc_mask(F, T, w, R, i, j))
+# Mask variants (or-ed; 0 = symmetric window, reference frames first,
+# reference queries global): see orc_mask.
+MASK_CAUSAL = 1
+MASK_REF_SUFFIX = 2
+MASK_REF_LOCAL = 4
 
 
-def mask_dense(F, T, w, R) -> np.ndarray:
+def mask(F, T, w, R, i, j, flags: int = 0) -> int:
+    return int(_load().orc_mask(F, T, w, R, flags, i, j))
+
+
+def mask_dense(F, T, w, R, flags: int = 0) -> np.ndarray:
     n = (F + R) * T
     out = np.zeros((n, n), dtype=np.uint8)
-    _load().orc_mask_dense(F, T, w, R, _ptr(out))
+    _load().orc_mask_dense(F, T, w, R, flags, _ptr(out))
     return out
 
 
-def blockmap(F, T, w, R, bq, bk) -> dict:
+def blockmap(F, T, w, R, bq, bk, flags: int = 0) -> dict:
     n = (F + R) * T
     if bq <= 0 or bk <= 0 or n % bq or n % bk:
         raise ValueError("block sizes must tile the sequence")
@@ -109,8 +116,8 @@ def blockmap(F, T, w, R, bq, bk) -> dict:
     row_ptr = np.zeros(nqb + 1, dtype=np.int32)
     col = np.zeros(nqb * nkb, dtype=np.int32)
     counts = np.zeros(4, dtype=np.int64)
-    rc = _load().orc_blockmap(F, T, w, R, bq, bk, _ptr(bitmap), _ptr(row_ptr), _ptr(col),
-                              nqb * nkb, _ptr(counts))
+    rc = _load().orc_blockmap(F, T, w, R, flags, bq, bk, _ptr(bitmap), _ptr(row_ptr),
+                              _ptr(col), nqb * nkb, _ptr(counts))
     if rc != 0:
         raise RuntimeError("orc_blockmap failed")
     nnz = int(counts[3])
@@ -130,15 +137,15 @@ def prepare(q, k, scale: float, tau: float = TAU) -> dict:
     return {"mu": mu, "kmax": kmax, "qn": qn, "b": b, "bmax": bmax, "elig": elig}
 
 
-def prepare_window(q, k, F, T, w, R, scale: float, tau: float = TAU) -> dict:
+def prepare_window(q, k, F, T, w, R, scale: float, tau: float = TAU, flags: int = 0) -> dict:
     """Like prepare(), with each row's bound over the keys its row attends
     (the mask walked element by element).  kmax stays the global maximum."""
     qd, kd = as_f64(q), as_f64(k)
     nbh, n, d = kd.shape
     mu = np.zeros((nbh, d)); kmax = np.zeros(nbh); qn = np.zeros((nbh, n))
     b = np.zeros((nbh, n)); bmax = np.zeros(nbh); elig = np.zeros(nbh, dtype=np.uint8)
-    _load().orc_prepare_window(_ptr(qd), _ptr(kd), nbh, n, d, F, T, w, R, scale, tau, _ptr(mu),
-                               _ptr(kmax), _ptr(qn), _ptr(b), _ptr(bmax), _ptr(elig))
+    _load().orc_prepare_window(_ptr(qd), _ptr(kd), nbh, n, d, F, T, w, R, flags, scale, tau,
+                               _ptr(mu), _ptr(kmax), _ptr(qn), _ptr(b), _ptr(bmax), _ptr(elig))
     return {"mu": mu, "kmax": kmax, "qn": qn, "b": b, "bmax": bmax, "elig": elig}
 
 
@@ -147,19 +154,19 @@ def _pairs(pairs):
     return np.ascontiguousarray(p[:, 0]), np.ascontiguousarray(p[:, 1])
 
 
-def attention_rows(q, k, v, F, T, w, R, scale, pairs) -> np.ndarray:
+def attention_rows(q, k, v, F, T, w, R, scale, pairs, flags: int = 0) -> np.ndarray:
     """Plain masked softmax attention for (head, row) pairs -> [npairs, D].
     Heads index the flattened [nbh] axis of q, k, v."""
     qd, kd, vd = as_f64(q), as_f64(k), as_f64(v)
     nbh, n, d = kd.shape
     h, r = _pairs(pairs)
     out = np.zeros((len(h), d))
-    _load().orc_attention_rows(_ptr(qd), _ptr(kd), _ptr(vd), n, d, F, T, w, R, scale, len(h),
-                               _ptr(h), _ptr(r), _ptr(out))
+    _load().orc_attention_rows(_ptr(qd), _ptr(kd), _ptr(vd), n, d, F, T, w, R, flags, scale,
+                               len(h), _ptr(h), _ptr(r), _ptr(out))
     return out
 
 
-def attention_rows_fixed(q, k, v, F, T, w, R, scale, pairs, stats) -> np.ndarray:
+def attention_rows_fixed(q, k, v, F, T, w, R, scale, pairs, stats, flags: int = 0) -> np.ndarray:
     qd, kd, vd = as_f64(q), as_f64(k), as_f64(v)
     nbh, n, d = kd.shape
     h, r = _pairs(pairs)
@@ -167,23 +174,23 @@ def attention_rows_fixed(q, k, v, F, T, w, R, scale, pairs, stats) -> np.ndarray
     b = np.ascontiguousarray(stats["b"], dtype=np.float64)
     out = np.zeros((len(h), d))
     _load().orc_attention_rows_fixed(_ptr(qd), _ptr(kd), _ptr(vd), _ptr(mu), _ptr(b), n, d, F,
-                                     T, w, R, scale, len(h), _ptr(h), _ptr(r), _ptr(out))
+                                     T, w, R, flags, scale, len(h), _ptr(h), _ptr(r), _ptr(out))
     return out
 
 
-def attention_rows_online(q, k, v, F, T, w, R, scale, bk, pairs) -> np.ndarray:
+def attention_rows_online(q, k, v, F, T, w, R, scale, bk, pairs, flags: int = 0) -> np.ndarray:
     qd, kd, vd = as_f64(q), as_f64(k), as_f64(v)
     nbh, n, d = kd.shape
     h, r = _pairs(pairs)
     out = np.zeros((len(h), d))
-    _load().orc_attention_rows_online(_ptr(qd), _ptr(kd), _ptr(vd), n, d, F, T, w, R, scale,
-                                      bk, len(h), _ptr(h), _ptr(r), _ptr(out))
+    _load().orc_attention_rows_online(_ptr(qd), _ptr(kd), _ptr(vd), n, d, F, T, w, R, flags,
+                                      scale, bk, len(h), _ptr(h), _ptr(r), _ptr(out))
     return out
 
 
-def attention_full(q, k, v, F, T, w, R, scale) -> np.ndarray:
+def attention_full(q, k, v, F, T, w, R, scale, flags: int = 0) -> np.ndarray:
     """Every row of every head: [nbh, N, D] (small shapes)."""
     kd = as_f64(k)
     nbh, n, d = kd.shape
     pairs = [(h, i) for h in range(nbh) for i in range(n)]
-    return attention_rows(q, k, v, F, T, w, R, scale, pairs).reshape(nbh, n, d)
+    return attention_rows(q, k, v, F, T, w, R, scale, pairs, flags).reshape(nbh, n, d)

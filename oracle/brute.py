@@ -16,28 +16,41 @@ def frame_of(tok: int, T: int) -> int:
     return tok // T
 
 
-def attends(i: int, j: int, T: int, w: int, R: int) -> bool:
+def attends(i: int, j: int, T: int, w: int, R: int, causal: bool = False,
+            ref_last: bool = False, ref_local: bool = False, F: int = 0) -> bool:
     """Query token i sees key token j: key in a reference frame, or query in a
-    reference frame, or the two video frames at most w apart."""
+    reference frame, or the two video frames at most w apart.  Variants:
+    causal (key frame at most w frames before, never after, the query's),
+    ref_last (the R reference frames come after the F video frames; F is
+    then needed), ref_local (reference queries see only reference keys)."""
     fi, fj = frame_of(i, T), frame_of(j, T)
-    if fj < R or fi < R:
+    if ref_last:
+        ref_i, ref_j, vi, vj = fi >= F, fj >= F, fi, fj
+    else:
+        ref_i, ref_j, vi, vj = fi < R, fj < R, fi - R, fj - R
+    if ref_i:
+        return ref_j if ref_local else True
+    if ref_j:
         return True
-    return abs((fi - R) - (fj - R)) <= w
+    if causal:
+        return 0 <= vi - vj <= w
+    return abs(vi - vj) <= w
 
 
-def mask(F: int, T: int, w: int, R: int):
+def mask(F: int, T: int, w: int, R: int, **variant):
     n = (F + R) * T
-    return [[1 if attends(i, j, T, w, R) else 0 for j in range(n)] for i in range(n)]
+    return [[1 if attends(i, j, T, w, R, F=F, **variant) else 0 for j in range(n)]
+            for i in range(n)]
 
 
-def attention(q, k, v, F, T, w, R, scale):
+def attention(q, k, v, F, T, w, R, scale, **variant):
     """q, k, v: nested lists [N][D] for one head.  Returns [N][D]."""
     n, d = len(q), len(q[0])
     out = []
     for i in range(n):
         logits = []
         for j in range(n):
-            if attends(i, j, T, w, R):
+            if attends(i, j, T, w, R, F=F, **variant):
                 logits.append((j, scale * sum(q[i][c] * k[j][c] for c in range(d))))
         top = max(s for _, s in logits)
         weights = [(j, math.exp(s - top)) for j, s in logits]

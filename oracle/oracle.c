@@ -48,22 +48,39 @@
 /* Mask element M[i, j] (1 = query token i attends key token j).
  * Reading: every query attends every reference key; reference queries are
  * global and attend every key; video queries attend video keys whose frame
- * index differs by at most w (clipped at the ends, no wrap-around). */
-int orc_mask(long F, long T, long w, long R, long i, long j) {
+ * index differs by at most w (clipped at the ends, no wrap-around).
+ * Variants of the same family (flags, or-ed; 0 = the reading above):
+ *   1  causal window: video frame f attends video frames f - w .. f;
+ *   2  the reference frames follow the F video frames in token order;
+ *   4  reference queries attend only reference keys. */
+int orc_mask(long F, long T, long w, long R, long flags, long i, long j) {
   long fi = i / T, fj = j / T;
-  (void)F;
-  if (fj < R) return 1;
-  if (fi < R) return 1;
-  long d = (fi - R) - (fj - R);
+  int ref_i, ref_j;
+  long vi, vj;
+  if (flags & 2) {
+    ref_i = fi >= F;
+    ref_j = fj >= F;
+    vi = fi;
+    vj = fj;
+  } else {
+    ref_i = fi < R;
+    ref_j = fj < R;
+    vi = fi - R;
+    vj = fj - R;
+  }
+  if (ref_i) return (flags & 4) ? ref_j : 1;
+  if (ref_j) return 1;
+  long d = vi - vj;
+  if (flags & 1) return (d >= 0 && d <= w) ? 1 : 0;
   if (d < 0) d = -d;
   return d <= w ? 1 : 0;
 }
 
 /* The whole N x N mask, element by element (small shapes only). */
-void orc_mask_dense(long F, long T, long w, long R, uint8_t* out) {
+void orc_mask_dense(long F, long T, long w, long R, long flags, uint8_t* out) {
   long n = (F + R) * T;
   for (long i = 0; i < n; ++i)
-    for (long j = 0; j < n; ++j) out[i * n + j] = (uint8_t)orc_mask(F, T, w, R, i, j);
+    for (long j = 0; j < n; ++j) out[i * n + j] = (uint8_t)orc_mask(F, T, w, R, flags, i, j);
 }
 
 /* Classifies every bq x bk block of the element mask.
@@ -71,7 +88,7 @@ void orc_mask_dense(long F, long T, long w, long R, uint8_t* out) {
  * CSR lists those blocks row by row in increasing kb.
  * counts[0..3] = full, empty, partial blocks, nonzero blocks.
  * Returns 0, or -1 when col_cap is too small or the sizes do not tile N. */
-int orc_blockmap(long F, long T, long w, long R, long bq, long bk, uint8_t* bitmap,
+int orc_blockmap(long F, long T, long w, long R, long flags, long bq, long bk, uint8_t* bitmap,
                  int32_t* row_ptr, int32_t* col, long col_cap, long* counts) {
   long n = (F + R) * T;
   if (bq <= 0 || bk <= 0 || n % bq != 0 || n % bk != 0) return -1;
@@ -82,7 +99,7 @@ int orc_blockmap(long F, long T, long w, long R, long bq, long bk, uint8_t* bitm
     for (long kb = 0; kb < nkb; ++kb) {
       long active = 0;
       for (long i = qb * bq; i < (qb + 1) * bq; ++i)
-        for (long j = kb * bk; j < (kb + 1) * bk; ++j) active += orc_mask(F, T, w, R, i, j);
+        for (long j = kb * bk; j < (kb + 1) * bk; ++j) active += orc_mask(F, T, w, R, flags, i, j);
       if (active == 0) {
         n_empty++;
         bitmap[qb * nkb + kb] = 0;
@@ -172,7 +189,7 @@ void orc_prepare(const double* q, const double* k, long nbh, long n, long d, dou
  *              (the mask walked element by element for every row);
  *   bmax, elig    from these b as in orc_prepare. */
 void orc_prepare_window(const double* q, const double* k, long nbh, long n, long d, long F,
-                        long T, long w, long R, double scale, double tau, double* mu,
+                        long T, long w, long R, long flags, double scale, double tau, double* mu,
                         double* kmax, double* qn, double* b, double* bmax, uint8_t* elig) {
   const double underflow_limit = 126.0 * log(2.0);
   double* knorm = (double*)malloc(sizeof(double) * (size_t)n * (size_t)nbh);
@@ -206,7 +223,7 @@ void orc_prepare_window(const double* q, const double* k, long nbh, long n, long
       qn[h * n + i] = sqrt(s);
       double kw = 0.0;
       for (long j = 0; j < n; ++j)
-        if (orc_mask(F, T, w, R, i, j) && kn[j] > kw) kw = kn[j];
+        if (orc_mask(F, T, w, R, flags, i, j) && kn[j] > kw) kw = kn[j];
       b[h * n + i] = scale * qn[h * n + i] * kw;
       if (b[h * n + i] > bm) bm = b[h * n + i];
       if (!(2.0 * b[h * n + i] < underflow_limit)) rows_ok = 0;
@@ -224,7 +241,7 @@ static double* row_scratch(long n) { return (double*)malloc((size_t)n * sizeof(d
  * s_ij = scale * q_i . k_j, A(i) = { j : M[i, j] = 1 }, for the listed
  * (head, row) pairs.  out is [npairs][D]. */
 void orc_attention_rows(const double* q, const double* k, const double* v, long n, long d,
-                        long F, long T, long w, long R, double scale, long npairs,
+                        long F, long T, long w, long R, long flags, double scale, long npairs,
                         const int64_t* head, const int64_t* row, double* out) {
 #pragma omp parallel
   {
@@ -237,7 +254,7 @@ void orc_attention_rows(const double* q, const double* k, const double* v, long 
       const double* vh = v + h * n * d;
       double mx = -INFINITY;
       for (long j = 0; j < n; ++j) {
-        if (!orc_mask(F, T, w, R, i, j)) continue;
+        if (!orc_mask(F, T, w, R, flags, i, j)) continue;
         double acc = 0.0;
         for (long c = 0; c < d; ++c) acc += qi[c] * kh[j * d + c];
         s[j] = scale * acc;
@@ -247,7 +264,7 @@ void orc_attention_rows(const double* q, const double* k, const double* v, long 
       double* o = out + p * d;
       for (long c = 0; c < d; ++c) o[c] = 0.0;
       for (long j = 0; j < n; ++j) {
-        if (!orc_mask(F, T, w, R, i, j)) continue;
+        if (!orc_mask(F, T, w, R, flags, i, j)) continue;
         double e = exp(s[j] - mx);
         den += e;
         for (long c = 0; c < d; ++c) o[c] += e * vh[j * d + c];
@@ -263,7 +280,7 @@ void orc_attention_rows(const double* q, const double* k, const double* v, long 
  * mu is [nbh][D], b is [nbh][N] (from orc_prepare). */
 void orc_attention_rows_fixed(const double* q, const double* k, const double* v,
                               const double* mu, const double* b, long n, long d, long F,
-                              long T, long w, long R, double scale, long npairs,
+                              long T, long w, long R, long flags, double scale, long npairs,
                               const int64_t* head, const int64_t* row, double* out) {
 #pragma omp parallel for schedule(dynamic, 4)
   for (long p = 0; p < npairs; ++p) {
@@ -277,7 +294,7 @@ void orc_attention_rows_fixed(const double* q, const double* k, const double* v,
     double* o = out + p * d;
     for (long c = 0; c < d; ++c) o[c] = 0.0;
     for (long j = 0; j < n; ++j) {
-      if (!orc_mask(F, T, w, R, i, j)) continue;
+      if (!orc_mask(F, T, w, R, flags, i, j)) continue;
       double acc = 0.0;
       for (long c = 0; c < d; ++c) acc += qi[c] * (kh[j * d + c] - m[c]);
       double e = exp(scale * acc - bi);
@@ -292,7 +309,8 @@ void orc_attention_rows_fixed(const double* q, const double* k, const double* v,
  * consecutive key indices; a running max m, and the running sum and output
  * rescaled by exp(m_old - m_new) whenever a block raises the max. */
 void orc_attention_rows_online(const double* q, const double* k, const double* v, long n,
-                               long d, long F, long T, long w, long R, double scale, long bk,
+                               long d, long F, long T, long w, long R, long flags, double scale,
+                               long bk,
                                long npairs, const int64_t* head, const int64_t* row,
                                double* out) {
 #pragma omp parallel
@@ -312,7 +330,7 @@ void orc_attention_rows_online(const double* q, const double* k, const double* v
         double bm = -INFINITY;
         int any = 0;
         for (long j = j0; j < j1; ++j) {
-          if (!orc_mask(F, T, w, R, i, j)) continue;
+          if (!orc_mask(F, T, w, R, flags, i, j)) continue;
           double acc = 0.0;
           for (long c = 0; c < d; ++c) acc += qi[c] * kh[j * d + c];
           s[j] = scale * acc;
@@ -325,7 +343,7 @@ void orc_attention_rows_online(const double* q, const double* k, const double* v
         l *= alpha;
         for (long c = 0; c < d; ++c) o[c] *= alpha;
         for (long j = j0; j < j1; ++j) {
-          if (!orc_mask(F, T, w, R, i, j)) continue;
+          if (!orc_mask(F, T, w, R, flags, i, j)) continue;
           double e = exp(s[j] - m_new);
           l += e;
           for (long c = 0; c < d; ++c) o[c] += e * vh[j * d + c];
