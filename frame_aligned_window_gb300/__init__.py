@@ -7,7 +7,7 @@ library.  If libwsattn.so is missing or fails to load, importing this
 package raises: there is no fallback implementation.
 
 The names mirror the C ABI:
-    wsattn_plan, wsattn_plan_destroy, wsattn_prepare, wsattn_forward,
+    wsattn_plan, wsattn_plan_ex, wsattn_plan_destroy, wsattn_prepare, wsattn_forward,
     wsattn_plan_info, wsattn_get_block_map, wsattn_get_csr, wsattn_get_stats,
     wsattn_plan_set_debug, wsattn_plan_set_bound, wsattn_device_status,
     wsattn_selftest_timeout, wsattn_status_string, wsattn_prepare_static
@@ -24,7 +24,7 @@ LIB_PATH = os.path.join(_HERE, "libwsattn.so")
 
 # C ABI entry points declared in include/wsattn.h
 EXPORTS = (
-    "wsattn_plan", "wsattn_plan_destroy", "wsattn_prepare", "wsattn_forward",
+    "wsattn_plan", "wsattn_plan_ex", "wsattn_plan_destroy", "wsattn_prepare", "wsattn_forward",
     "wsattn_plan_info", "wsattn_get_block_map", "wsattn_get_csr", "wsattn_get_stats",
     "wsattn_plan_set_debug", "wsattn_plan_set_bound", "wsattn_device_status",
     "wsattn_selftest_timeout", "wsattn_status_string", "wsattn_prepare_static",
@@ -33,6 +33,11 @@ EXPORTS = (
 # wsattn_bound
 BOUND_GLOBAL = 0
 BOUND_WINDOW = 1
+
+# wsattn_mask_flags (or-ed)
+MASK_CAUSAL = 1
+MASK_REF_SUFFIX = 2
+MASK_REF_LOCAL = 4
 
 STATUS = {0: "OK", 1: "BAD_ARG", 2: "BAD_BLOCK", 3: "UNSUPPORTED", 4: "NOT_PREPARED",
           5: "BATCH_MISMATCH", 6: "CUDA", 7: "TIMEOUT", 8: "NO_MEMORY"}
@@ -51,6 +56,7 @@ _lib = ctypes.CDLL(LIB_PATH)
 
 _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
 _lib.wsattn_plan.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_P)]
+_lib.wsattn_plan_ex.argtypes = [_I, _I, _I, _I, _I, _I, _I, _I, _I, ctypes.POINTER(_P)]
 _lib.wsattn_plan_destroy.argtypes = [_P]
 _lib.wsattn_prepare.argtypes = [_P, _I, _P, _P, _P]
 _lib.wsattn_forward.argtypes = [_P, _I, _P, _P, _P, _P, _P]
@@ -139,11 +145,23 @@ def _check_shape(plan: Plan, t, name):
 
 
 def wsattn_plan(frames, tokens_per_frame, window, ref_frames, heads, head_dim, block_q=0,
-                block_k=0) -> Plan:
+                block_k=0, mask_flags=0) -> Plan:
+    """wsattn_plan_ex when mask_flags != 0 (MASK_* or-ed), else wsattn_plan."""
     h = _P()
     args = (frames, tokens_per_frame, window, ref_frames, heads, head_dim, block_q, block_k)
-    _check(_lib.wsattn_plan(*args, ctypes.byref(h)), "wsattn_plan")
-    return Plan(h, args)
+    if mask_flags:
+        _check(_lib.wsattn_plan_ex(*args, int(mask_flags), ctypes.byref(h)), "wsattn_plan_ex")
+    else:
+        _check(_lib.wsattn_plan(*args, ctypes.byref(h)), "wsattn_plan")
+    plan = Plan(h, args)
+    plan.mask_flags = int(mask_flags)
+    return plan
+
+
+def wsattn_plan_ex(frames, tokens_per_frame, window, ref_frames, heads, head_dim, block_q,
+                   block_k, mask_flags) -> Plan:
+    return wsattn_plan(frames, tokens_per_frame, window, ref_frames, heads, head_dim, block_q,
+                       block_k, mask_flags)
 
 
 def wsattn_plan_destroy(plan: Plan):

@@ -163,12 +163,18 @@ extern "C" {
 
 int wsattn_plan(int frames, int tokens_per_frame, int window, int ref_frames, int heads,
                 int head_dim, int block_q, int block_k, wsattn_plan_t* out) {
+  return wsattn_plan_ex(frames, tokens_per_frame, window, ref_frames, heads, head_dim, block_q,
+                        block_k, 0, out);
+}
+
+int wsattn_plan_ex(int frames, int tokens_per_frame, int window, int ref_frames, int heads,
+                   int head_dim, int block_q, int block_k, int mask_flags, wsattn_plan_t* out) {
   if (!out) return WSATTN_ERR_BAD_ARG;
   *out = nullptr;
   wsattn_plan_s* p = new (std::nothrow) wsattn_plan_s();
   if (!p) return WSATTN_ERR_NO_MEMORY;
   const int rc = wsattn::build_host_plan(frames, tokens_per_frame, window, ref_frames, heads,
-                                         head_dim, block_q, block_k, &p->hp);
+                                         head_dim, block_q, block_k, mask_flags, &p->hp);
   if (rc != WSATTN_OK) {
     delete p;
     return rc;
@@ -195,7 +201,7 @@ int wsattn_prepare(wsattn_plan_t plan, int batch, const void* q, const void* k, 
   if (rc != WSATTN_OK) return rc;
   const int BH = batch * hp.H;
   int nchunk = 0, rpc = 0;
-  wsattn::FrameWindow win{hp.F + hp.R, hp.R, hp.w};
+  wsattn::FrameWindow win{hp.F + hp.R, hp.F, hp.R, hp.w, hp.flags};
   const bool window = plan->bound_mode == WSATTN_BOUND_WINDOW;
   if (window) {
     nchunk = win.nf;  // one chunk per frame: its maxima are the frame's

@@ -45,6 +45,7 @@ struct WorkTile {
 // Host-side plan: geometry, block map, and the forward work list.
 struct HostPlan {
   int F = 0, T = 0, w = 0, R = 0, H = 0, D = 0, bq = 0, bk = 0;
+  int flags = 0;                   // wsattn_mask_flags
   int64_t N = 0, nqb = 0, nkb = 0;
   std::vector<uint8_t> bitmap;     // [nqb * nkb]
   std::vector<int32_t> row_ptr;    // [nqb + 1]
@@ -62,7 +63,20 @@ struct HostPlan {
 
 // Builds everything above; returns a WSATTN_* status.
 int build_host_plan(int frames, int tokens_per_frame, int window, int ref_frames, int heads,
-                    int head_dim, int block_q, int block_k, HostPlan* out);
+                    int head_dim, int block_q, int block_k, int mask_flags, HostPlan* out);
+
+// Frame rule of the mask family: query frame a attends key frame c (frame
+// indices in token order).  Host and device share it.
+__host__ __device__ inline bool frames_interact(int a, int c, int F, int w, int R, int flags) {
+  const bool suffix = (flags & WSATTN_MASK_REF_SUFFIX) != 0;
+  const bool ref_a = suffix ? a >= F : a < R;
+  const bool ref_c = suffix ? c >= F : c < R;
+  if (ref_a) return (flags & WSATTN_MASK_REF_LOCAL) ? ref_c : true;
+  if (ref_c) return true;
+  const int d = a - c;  // video indices differ by the same amount as frame indices
+  if (flags & WSATTN_MASK_CAUSAL) return d >= 0 && d <= w;
+  return (d < 0 ? -d : d) <= w;
+}
 
 // Picks a block size for T: among the valid sizes (multiples of 16 dividing
 // T, at most kStepKeys), the one whose forward key step
@@ -85,11 +99,13 @@ struct PrepBuffers {
 };
 
 // Frame structure for window bounds: chunk c of a head is frame c (T rows),
-// and query frame a attends key frame g iff g < R, a < R or |a - g| <= w.
+// and query frame a attends key frame g as frames_interact says.
 struct FrameWindow {
   int nf;  // R + F frames (= chunks per head)
+  int F;
   int R;
   int w;
+  int flags;  // wsattn_mask_flags
 };
 
 // Enqueues the three prepare passes; returns a cudaError_t.  With `win`

@@ -7,9 +7,12 @@
 // entirely active or entirely skipped.  The map is built at frame granularity
 // and expanded to blocks; no element of the mask is ever materialised.
 //
-// Frame rule (token-order frame indices; reference frames are the prefix):
+// Frame rule (frames_interact in internal.h; token-order frame indices):
 // query frame a sees key frame c iff c is a reference frame, a is a reference
-// frame (reference queries are global), or |(a - R) - (c - R)| <= w.
+// frame (reference queries are global), or the video frames are at most w
+// apart; the mask variants make the window causal (c in a - w .. a), move the
+// reference frames after the video frames, or confine reference queries to
+// reference keys.
 #include <algorithm>
 #include <new>
 
@@ -35,16 +38,11 @@ int auto_block(int T) {
   return best;
 }
 
-static bool frames_interact(int a, int c, int w, int R) {
-  if (c < R || a < R) return true;
-  int d = a - c;
-  if (d < 0) d = -d;
-  return d <= w;
-}
-
 int build_host_plan(int frames, int tokens_per_frame, int window, int ref_frames, int heads,
-                    int head_dim, int block_q, int block_k, HostPlan* out) {
+                    int head_dim, int block_q, int block_k, int mask_flags, HostPlan* out) {
   if (!out) return WSATTN_ERR_BAD_ARG;
+  const int all_flags = WSATTN_MASK_CAUSAL | WSATTN_MASK_REF_SUFFIX | WSATTN_MASK_REF_LOCAL;
+  if (mask_flags & ~all_flags) return WSATTN_ERR_BAD_ARG;
   if (frames < 1 || ref_frames < 0 || window < 0 || heads < 1) return WSATTN_ERR_BAD_ARG;
   if (tokens_per_frame < 16 || tokens_per_frame % 16 != 0) return WSATTN_ERR_BAD_BLOCK;
   if (head_dim != 64 && head_dim != 128) return WSATTN_ERR_UNSUPPORTED;
@@ -61,6 +59,7 @@ int build_host_plan(int frames, int tokens_per_frame, int window, int ref_frames
   HostPlan& p = *out;
   p = HostPlan{};
   p.F = frames; p.T = T; p.w = window; p.R = ref_frames; p.H = heads; p.D = head_dim;
+  p.flags = mask_flags;
   p.bq = bq; p.bk = bk; p.N = N;
   p.nqb = N / bq;
   p.nkb = N / bk;
@@ -73,7 +72,7 @@ int build_host_plan(int frames, int tokens_per_frame, int window, int ref_frames
       const int a = static_cast<int>(qb * bq / T);
       for (int64_t kb = 0; kb < p.nkb; ++kb) {
         const int c = static_cast<int>(kb * bk / T);
-        if (frames_interact(a, c, window, ref_frames)) {
+        if (frames_interact(a, c, frames, window, ref_frames, mask_flags)) {
           p.bitmap[static_cast<size_t>(qb * p.nkb + kb)] = 1;
           p.col.push_back(static_cast<int32_t>(kb));
         }
@@ -84,7 +83,9 @@ int build_host_plan(int frames, int tokens_per_frame, int window, int ref_frames
     int64_t pairs = 0;
     for (int64_t a = 0; a < nf; ++a)
       for (int64_t c = 0; c < nf; ++c)
-        if (frames_interact(static_cast<int>(a), static_cast<int>(c), window, ref_frames)) pairs++;
+        if (frames_interact(static_cast<int>(a), static_cast<int>(c), frames, window, ref_frames,
+                            mask_flags))
+          pairs++;
     p.active_pairs = pairs * T * T;
 
     // Work list: every 128-row query tile of every frame, with the frame's key

@@ -229,7 +229,8 @@ __global__ void __launch_bounds__(kPrepThreads)
 // B_h = max_a (scale max_{i in a} ||q_i||) K_a, which equals max_i b_i (the
 // expression is monotone in ||q_i||).  kmax keeps the head's global maximum.
 __global__ void __launch_bounds__(kPrepThreads)
-    prep_pass_c_window(int64_t n, int rpc, int nchunk, int R, int w, float scale, float tau,
+    prep_pass_c_window(int64_t n, int rpc, int nchunk, int F, int R, int w, int flags,
+                       float scale, float tau,
                        float* __restrict__ b_rows, float* __restrict__ m_rows,
                        const float* __restrict__ part_kmax, const float* __restrict__ part_qmax,
                        float* __restrict__ kmax, float* __restrict__ bmax,
@@ -239,10 +240,8 @@ __global__ void __launch_bounds__(kPrepThreads)
   const float* pk = part_kmax + static_cast<size_t>(bh) * nchunk;
   auto window_max = [&](int f) {
     float kh = 0.f;
-    for (int g = 0; g < nchunk; ++g) {
-      const int d = f > g ? f - g : g - f;
-      if (g < R || f < R || d <= w) kh = fmaxf(kh, pk[g]);
-    }
+    for (int g = 0; g < nchunk; ++g)
+      if (frames_interact(f, g, F, w, R, flags)) kh = fmaxf(kh, pk[g]);
     return kh;
   };
   if (threadIdx.x == 0) k_s = window_max(a);
@@ -304,7 +303,8 @@ cudaError_t launch_prepare(const void* q, const void* k, int BH, int64_t N, int 
   }
   if (win)
     prep_pass_c_window<<<grid, kPrepThreads, 0, stream>>>(
-        N, b.rows_per_chunk, b.nchunk, win->R, win->w, scale, tau, b.b_rows, b.m_rows,
+        N, b.rows_per_chunk, b.nchunk, win->F, win->R, win->w, win->flags, scale, tau, b.b_rows,
+        b.m_rows,
         b.part_kmax, b.part_qmax, b.kmax, b.bmax, b.elig);
   else
     prep_pass_c<<<grid, kPrepThreads, 0, stream>>>(N, b.rows_per_chunk, b.nchunk, scale, tau,

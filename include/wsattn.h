@@ -85,6 +85,22 @@ typedef struct wsattn_plan_s* wsattn_plan_t;
 int wsattn_plan(int frames, int tokens_per_frame, int window, int ref_frames, int heads,
                 int head_dim, int block_q, int block_k, wsattn_plan_t* out);
 
+/* Variants of the mask family (or-ed into mask_flags; 0 = the mask described
+ * at the top of this file).  Every variant keeps each frame's active key
+ * blocks in at most two runs, so the same kernels run it unchanged. */
+enum wsattn_mask_flags {
+  WSATTN_MASK_CAUSAL = 1,     /* video frame f attends video frames f - w .. f only */
+  WSATTN_MASK_REF_SUFFIX = 2, /* the R reference frames follow the F video frames */
+  WSATTN_MASK_REF_LOCAL = 4   /* reference queries attend only reference keys */
+};
+
+/* wsattn_plan with a mask variant.  wsattn_plan(...) is
+ * wsattn_plan_ex(..., 0, out).  With WSATTN_MASK_REF_SUFFIX the token order
+ * is video frames 0..F-1, then the reference frames.
+ * Errors: as wsattn_plan; BAD_ARG for unknown flag bits. */
+int wsattn_plan_ex(int frames, int tokens_per_frame, int window, int ref_frames, int heads,
+                   int head_dim, int block_q, int block_k, int mask_flags, wsattn_plan_t* out);
+
 /* Releases the plan and every host and device buffer it owns.  The caller
  * must make sure no work that uses the plan is still running on the GPU.
  * NULL is accepted and ignored. */

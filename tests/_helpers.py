@@ -42,11 +42,13 @@ def oracle_prepare_all(wl, q, k, chunk=8, tau=oracle.TAU) -> dict:
     return {key: np.concatenate([p[key] for p in parts]) for key in parts[0]}
 
 
-def gpu_run(wl, q, k, v, block_k=0, force_path=-1, tau=0.0):
+def gpu_run(wl, q, k, v, block_k=0, force_path=-1, tau=0.0, mask_flags=0, bound=0):
     """Plan, prepare and forward through the library; returns (plan, out, k_centered)."""
     import frame_aligned_window_gb300 as fw
     plan = fw.wsattn_plan(wl.frames, wl.tokens_per_frame, wl.window, wl.ref_frames, wl.heads,
-                          wl.head_dim, 0, block_k)
+                          wl.head_dim, 0, block_k, mask_flags)
+    if bound:
+        fw.wsattn_plan_set_bound(plan, bound)
     if force_path >= 0 or tau > 0:
         fw.wsattn_plan_set_debug(plan, force_path, tau)
     qd, kd, vd = q.cuda(), k.cuda(), v.cuda()

@@ -43,17 +43,17 @@ def valid_blocks(T, cap=None):
     return [b for b in range(16, (cap or T) + 1, 16) if T % b == 0]
 
 
-def _plan_vs_oracle(F, T, w, R, bq, bk):
+def _plan_vs_oracle(F, T, w, R, bq, bk, flags=0):
     import frame_aligned_window_gb300 as fw
-    plan = fw.wsattn_plan(F, T, w, R, 2, 128, bq, bk)
-    want = oracle.blockmap(F, T, w, R, bq, bk)
+    plan = fw.wsattn_plan(F, T, w, R, 2, 128, bq, bk, flags)
+    want = oracle.blockmap(F, T, w, R, bq, bk, flags)
     assert want["partial"] == 0
     np.testing.assert_array_equal(fw.wsattn_get_block_map(plan), want["bitmap"])
     rp, col = fw.wsattn_get_csr(plan)
     np.testing.assert_array_equal(rp, want["row_ptr"])
     np.testing.assert_array_equal(col, want["col"])
     assert plan.nnz == want["nnz"]
-    m_pairs = oracle.blockmap(F, T, w, R, T, T)["nnz"] * T * T
+    m_pairs = oracle.blockmap(F, T, w, R, T, T, flags)["nnz"] * T * T
     assert plan.active_pairs == m_pairs
     assert plan.tiles_per_head == (F + R) * ((T + 127) // 128)
     plan.destroy()
@@ -65,6 +65,20 @@ def test_plan_matches_oracle_all_valid_sizes(name):
     T = wl.tokens_per_frame
     for bq, bk in itertools.product(valid_blocks(T), valid_blocks(T)):
         _plan_vs_oracle(wl.frames, T, wl.window, wl.ref_frames, bq, bk)
+
+
+@pytest.mark.parametrize("flags", [1, 2, 3, 4, 5, 6, 7])
+@pytest.mark.parametrize("F,T,w,R,bq,bk", [(4, 48, 1, 1, 16, 48), (7, 32, 2, 2, 32, 16),
+                                           (5, 16, 9, 1, 16, 16), (6, 32, 0, 0, 32, 32)])
+def test_plan_matches_oracle_mask_variants(flags, F, T, w, R, bq, bk):
+    _plan_vs_oracle(F, T, w, R, bq, bk, flags)
+
+
+def test_plan_rejects_unknown_mask_flags():
+    import frame_aligned_window_gb300 as fw
+    with pytest.raises(fw.WsattnError) as e:
+        fw.wsattn_plan(4, 48, 1, 1, 2, 64, 0, 0, 8)
+    assert e.value.code == 1
 
 
 @pytest.mark.parametrize("bq,bk", [(80, 80), (16, 208), (1040, 80), (208, 16)])
