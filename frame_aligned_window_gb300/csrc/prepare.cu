@@ -271,8 +271,10 @@ __global__ void __launch_bounds__(kPrepThreads)
 }  // namespace
 
 void prepare_chunking(int BH, int64_t N, int num_sms, int* nchunk, int* rows_per_chunk) {
-  // About four waves of CTAs over the GPU, at least 64 rows per CTA.
-  int64_t want = (4LL * num_sms + BH - 1) / BH;
+  // One wave of pass B (its registers fit three 256-thread CTAs per SM):
+  // 3 * SMs CTAs over the heads, at least 64 rows per CTA.  A partial second
+  // wave would leave most SMs idle for its whole length.
+  int64_t want = 3LL * num_sms / BH;
   int64_t max_chunks = (N + 63) / 64;
   if (want > max_chunks) want = max_chunks;
   if (want < 1) want = 1;
