@@ -228,3 +228,34 @@ def test_bounded_wait_reports_timeout():
     assert fw.wsattn_selftest_timeout(20) == 7
     x = torch.ones(4, device="cuda")
     assert float(x.sum()) == 4.0
+
+
+def test_sr_shape_block16_full_size_sampled():
+    # The SR workload with 16-key blocks: 160-key steps of ten blocks, loaded
+    # as one box per slab like the 80-key-block steps.
+    wl = workload("sr")
+    q, k, v = generate(wl)
+    _, out, _ = gpu_run(wl, q, k, v, block_k=16)
+    _sampled_compare(wl, q, k, v, out)
+
+
+def test_sr_shape_batch2_d64_sampled():
+    # Batch 2, head dim 64, the SR frame structure (6 heads, 8 + 1 frames).
+    wl, q, k, v = micro(140, 2, 6, 64, 8, 1, 1040, 2)
+    _, out, _ = gpu_run(wl, q, k, v)
+    bh = [(0, 0), (1, 5)]
+    rows = sample_rows(wl, n_random=128)
+    want = oracle_rows(wl, q, k, v, bh, rows)
+    got = torch.stack([out[b, h, rows] for b, h in bh]).cpu().double().numpy()
+    _check(got, want, "sr-shape batch 2, D=64")
+
+
+@pytest.mark.parametrize("name", ["sr", "dense"])
+def test_window_bound_full_size_sampled(name):
+    import frame_aligned_window_gb300 as fw
+    wl = workload(name)
+    q, k, v = generate(wl)
+    plan, out, _ = gpu_run(wl, q, k, v, bound=fw.BOUND_WINDOW)
+    st = fw.wsattn_get_stats(plan, wl.batch)
+    assert st["elig"].all()
+    _sampled_compare(wl, q, k, v, out)
