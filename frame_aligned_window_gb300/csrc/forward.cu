@@ -20,10 +20,11 @@
 //               tcgen05.mma kind::f16 (bf16 in, fp32 accumulate in TMEM).
 //               Q and P are read from TMEM, K and V from shared memory.
 //   warp 2      allocates and frees tensor memory.
-//   warps 4-11  two softmax + epilogue warpgroups.  Thread i of a warpgroup
-//               owns row i of the tile (TMEM lane i); warpgroup 0 takes the
-//               first s columns of every key step, warpgroup 1 the rest
-//               (s = 16 * ceil(keys / 32)), so each SMSP runs two softmax warps.
+//   warps 4-11  two softmax + epilogue warpgroups (kNumWG).  Thread i of a
+//               warpgroup owns row i of the tile (TMEM lane i); the 16-column
+//               chunks of a key step are split over the warpgroups in order
+//               (warpgroup 0 takes ceil(chunks / 2)), so each SMSP runs two
+//               softmax warps.
 //
 // Keys are consumed in steps of up to G consecutive active blocks of one run
 // (G * bk <= 160 keys): the step's rows are consecutive, so K and V arrive as
@@ -56,10 +57,11 @@ namespace {
 
 using namespace ptx;
 
-constexpr int kThreads = 384;
+constexpr int kNumWG = 2;  // softmax warpgroups (3 and 4 measured slower: more arrivals, fewer registers)
 constexpr int kSoftmaxWarp0 = 4;
-constexpr int kSoftmaxWarps = 8;
-constexpr int kMaxChunksAll = 5;  // 16-column chunks a warpgroup takes at 160 keys
+constexpr int kSoftmaxWarps = 4 * kNumWG;
+constexpr int kThreads = 32 * (kSoftmaxWarp0 + kSoftmaxWarps);
+constexpr int kMaxChunksAll = (10 + kNumWG - 1) / kNumWG;   // chunks a warpgroup takes at 160 keys
 constexpr long long kWaitLimitCycles = 1LL << 31;  // about one second
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint32_t kTmemCols = 512;
@@ -84,14 +86,14 @@ enum : int {
   B_VEMPTY0 = B_VFULL0 + 4,
   B_COUNT = B_VEMPTY0 + 4
 };
-// Exchange area after the barriers: row maxima and row sums of the two
-// warpgroups, double-buffered: float [2 parity][2 warpgroups][128 rows] each.
-constexpr uint32_t kXchBytes = 2 * 2 * 2 * 128 * 4;
+// Exchange area after the barriers: row maxima and row sums of the
+// warpgroups, double-buffered: float [2 parity][kNumWG][128 rows] each.
+constexpr uint32_t kXchBytes = 2 * 2 * kNumWG * 128 * 4;
 
 struct Shared {
   uint32_t q, k, v, bars;  // shared-window addresses
-  float* xch_m;            // [2][2][128]
-  float* xch_l;            // [2][2][128]
+  float* xch_m;            // [2][kNumWG][128]
+  float* xch_l;            // [2][kNumWG][128]
   volatile int* abort_flag;
   int* status;
 };
@@ -146,9 +148,16 @@ __device__ __forceinline__ bool xch_sync(const Shared& s, uint32_t& xc) {
   return ok;
 }
 
-// First S column of warpgroup 1 in a step of `keys` keys (its P starts at
-// column s/2 of the P buffer).
-__device__ __forceinline__ int split_col(int keys) { return 16 * ((keys / 16 + 1) / 2); }
+// The share of warpgroup w when n units (16-column chunks of a key step, or
+// 16-element groups of D) are split over the warpgroups: the earlier
+// warpgroups take the larger shares; first = units before w's.
+__device__ __forceinline__ void wg_share(int n, int w, int& first, int& count) {
+  first = 0;
+#pragma unroll
+  for (int v = 0; v < kNumWG - 1; ++v)
+    if (v < w) first += (n + kNumWG - 1 - v) / kNumWG;
+  count = (n + kNumWG - 1 - w) / kNumWG;
+}
 
 // Tensor-memory columns: O [0, D), S [D, D + step), P buffers of step/2
 // columns from D + step, Q (D/2 columns) after them.
@@ -368,7 +377,7 @@ __device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
       // 16 key rows (2 KB of V, 8 P columns) per k-step
       mma_ts(t_o, a_p, vd, id_pv, j > 0 ? 1u : 0u);
 #pragma unroll
-      for (int kk = 1; kk < 2 * MAXC; ++kk)
+      for (int kk = 1; kk < kNumWG * MAXC; ++kk)
         if (kk < nks) mma_ts(t_o, a_p + kk * 8, vd + kk * 128, id_pv, 1u);
       tc_commit(bar(s, B_VEMPTY0 + vslot));
       tc_commit(bar(s, B_PVDONE0 + pb));
@@ -381,17 +390,20 @@ __device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
 }
 
 // -------------------------------------------------------------- softmax WGs
-// Copies this thread's share of its Q row (elements [wg D/2, (wg+1) D/2))
-// from the swizzled staging tile into TMEM (column c holds elements 2c and
-// 2c+1); rows past the frame are zeroed.
+// Copies this thread's share of its Q row (the warpgroup's 16-element groups
+// of D) from the swizzled staging tile into TMEM (column c holds elements 2c
+// and 2c+1); rows past the frame are zeroed.
 template <int D>
 __device__ bool load_q(const Shared& s, uint32_t t_q, int wg, int r, int nvalid, uint32_t& qc) {
   if (!wait_warp(s, bar(s, B_QFULL), qc & 1u)) return false;
   ++qc;
   const bool zero = r >= nvalid;
+  int g0, ng;
+  wg_share(D / 16, wg, g0, ng);
 #pragma unroll
-  for (int h = 0; h < D / 32; ++h) {
-    const int e0 = wg * (D / 2) + 16 * h;  // first element of this 16-element group
+  for (int h = 0; h < (D / 16 + kNumWG - 1) / kNumWG; ++h) {
+    if (h >= ng) break;
+    const int e0 = 16 * (g0 + h);  // first element of this 16-element group
     const uint32_t row_addr = s.q + (e0 / 64) * (kTileM * 128) + r * 128;
     uint32_t w[8];
 #pragma unroll
@@ -465,7 +477,9 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
   const uint32_t lane = tbase + (static_cast<uint32_t>((warp & 3) * 32) << 16);
   const int bk = p.bk, G = p.G;
   const TmemCols tc_ = tmem_cols<D>(G * bk);
-  const uint32_t ocol = tc_.o + static_cast<uint32_t>(wg * (D / 2));  // this WG's O half
+  int og0, nog;  // this warpgroup's 16-column groups of O
+  wg_share(D / 16, wg, og0, nog);
+  const uint32_t ocol = tc_.o + static_cast<uint32_t>(16 * og0);
   const float c = p.scale_log2;
   const uint64_t c2 = f2_pack(c, c);
   const int n_items = p.n_tiles * p.bh;
@@ -496,9 +510,9 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         int nblk;
         st.next(G, nblk);
         const int keys = nblk * bk;
-        const int split = split_col(keys);
-        const uint32_t c0 = wg == 0 ? 0u : static_cast<uint32_t>(split);  // first S column
-        const int n16 = (wg == 0 ? split : keys - split) / 16;           // 16-column chunks
+        int f16, n16;  // this warpgroup's 16-column chunks of the step
+        wg_share(keys / 16, wg, f16, n16);
+        const uint32_t c0 = static_cast<uint32_t>(16 * f16);  // first S column
         if (!wait_warp(s, bar(s, B_SFULL), su)) return;
         tc_fence_after();
         uint32_t sv[MAXC][16];
@@ -523,9 +537,9 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         int nblk;
         st.next(G, nblk);
         const int keys = nblk * bk;
-        const int split = split_col(keys);
-        const uint32_t c0 = wg == 0 ? 0u : static_cast<uint32_t>(split);
-        const int n16 = (wg == 0 ? split : keys - split) / 16;
+        int f16, n16;
+        wg_share(keys / 16, wg, f16, n16);
+        const uint32_t c0 = static_cast<uint32_t>(16 * f16);
         if (!wait_warp(s, bar(s, B_SFULL), su)) return;
         tc_fence_after();
         uint32_t sv[MAXC][16];
@@ -542,11 +556,13 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
             for (int i = 0; i < 16; ++i) mx = fmaxf(mx, __uint_as_float(sv[k][i]));
           }
         }
-        s.xch_m[(xpar * 2 + wg) * kTileM + r] = mx;
+        s.xch_m[(xpar * kNumWG + wg) * kTileM + r] = mx;
         if (!xch_sync(s, xc)) return;
-        const float mo = s.xch_m[(xpar * 2 + (wg ^ 1)) * kTileM + r];
+        float mall = mx;
+#pragma unroll
+        for (int v = 0; v < kNumWG; ++v) mall = fmaxf(mall, s.xch_m[(xpar * kNumWG + v) * kTileM + r]);
         xpar ^= 1u;
-        const float m_new = fmaxf(m, fmaxf(mx, mo) * c);
+        const float m_new = fmaxf(m, mall * c);
         const float alpha = ex2_approx(m - m_new);
         const uint32_t pb = pr.slot;
         if (!wait_warp(s, bar(s, B_PVDONE0 + pb), pr.phase ^ 1u)) return;
@@ -565,7 +581,7 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
           if (__any_sync(0xffffffffu, alpha < 1.f)) {
             const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
-            for (int k = 0; k < D / 32; ++k) {
+            for (int k = 0; k < nog; ++k) {
               uint32_t ra[16];
               tmem_ld16(lane + ocol + k * 16, ra);
               tmem_wait_ld16(ra);
@@ -594,17 +610,19 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
       return;
 
     if (!wait_warp(s, bar(s, B_OFULL), tiles_done & 1u)) return;
-    // the row sum is the sum of the two warpgroups' partial sums
+    // the row sum is the sum of the warpgroups' partial sums (fixed order)
     const uint32_t lpar = tiles_done & 1u;
     ++tiles_done;
-    s.xch_l[(lpar * 2 + wg) * kTileM + r] = l;
+    s.xch_l[(lpar * kNumWG + wg) * kTileM + r] = l;
     if (!xch_sync(s, xc)) return;
-    const float lsum = s.xch_l[(lpar * 2 + 0) * kTileM + r] + s.xch_l[(lpar * 2 + 1) * kTileM + r];
+    float lsum = 0.f;
+#pragma unroll
+    for (int v = 0; v < kNumWG; ++v) lsum += s.xch_l[(lpar * kNumWG + v) * kTileM + r];
     tc_fence_after();
     const float inv = 1.f / lsum;
-    float* orow = p.out + grow * D + wg * (D / 2);
+    float* orow = p.out + grow * D + 16 * og0;
 #pragma unroll 1
-    for (int k = 0; k < D / 32; ++k) {
+    for (int k = 0; k < nog; ++k) {
       uint32_t v[16];
       tmem_ld16(lane + ocol + k * 16, v);
       tmem_wait_ld16(v);
@@ -623,7 +641,7 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
 }
 
 // -------------------------------------------------------------------- kernel
-// MAXC = 16-column chunks per warpgroup and key step: ceil(G * bk / 32).
+// MAXC = 16-column chunks per warpgroup and key step: ceil(G * bk / 16 / kNumWG).
 template <int D, int MAXC>
 __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_constant__ FwdParams p) {
   extern __shared__ uint8_t smem_raw[];
@@ -637,7 +655,7 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
   s.bars = s.v + static_cast<uint32_t>(p.stages_v) * stage_bytes;
   uint8_t* gbars = smem_raw + (s.bars - raw);
   s.xch_m = reinterpret_cast<float*>(gbars + 8 * B_COUNT + 16);
-  s.xch_l = s.xch_m + 2 * 2 * kTileM;
+  s.xch_l = s.xch_m + 2 * kNumWG * kTileM;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(gbars + 8 * B_COUNT);
   s.abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   s.status = p.status;
@@ -726,16 +744,20 @@ cudaError_t launch_one(const FwdParams& p, int grid, size_t smem, cudaStream_t s
   return cudaGetLastError();
 }
 
+template <int D, int M>
+cudaError_t launch_m(const FwdParams& p, int maxc, int grid, size_t smem, cudaStream_t stream) {
+  if constexpr (M > kMaxChunksAll) {
+    return cudaErrorInvalidValue;
+  } else {
+    if (maxc == M) return launch_one<D, M>(p, grid, smem, stream);
+    return launch_m<D, M + 1>(p, maxc, grid, smem, stream);
+  }
+}
+
 template <int D>
 cudaError_t launch_d(const FwdParams& p, int grid, size_t smem, cudaStream_t stream) {
-  switch ((p.G * p.bk + 31) / 32) {
-    case 1: return launch_one<D, 1>(p, grid, smem, stream);
-    case 2: return launch_one<D, 2>(p, grid, smem, stream);
-    case 3: return launch_one<D, 3>(p, grid, smem, stream);
-    case 4: return launch_one<D, 4>(p, grid, smem, stream);
-    case 5: return launch_one<D, 5>(p, grid, smem, stream);
-    default: return cudaErrorInvalidValue;
-  }
+  const int chunks = p.G * p.bk / 16;  // 16-column chunks of a full step
+  return launch_m<D, 1>(p, (chunks + kNumWG - 1) / kNumWG, grid, smem, stream);
 }
 
 }  // namespace
@@ -754,7 +776,7 @@ void forward_stages(int D, int step_keys, size_t smem_optin, int* stages_k, int*
 }
 
 cudaError_t launch_forward(const FwdParams& p, int D, int grid, size_t smem, cudaStream_t stream) {
-  static_assert(kMaxChunksAll * 32 >= kStepKeys, "chunk instantiations must cover a step");
+  static_assert(kMaxChunksAll * 16 * kNumWG >= kStepKeys, "chunk instantiations must cover a step");
   return D == 128 ? launch_d<128>(p, grid, smem, stream) : launch_d<64>(p, grid, smem, stream);
 }
 
