@@ -54,6 +54,19 @@ bool get_encode() {
 bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; }
 
 // 2-D view [rows, D] of a bf16 tensor; box {64, box_rows}; 128-byte swizzle.
+// fp32 [rows, D] output, box {16 columns, 32 rows}: one softmax warp's
+// normalised rows of one 16-column group.
+bool encode_out_map(CUtensorMap* m, void* ptr, int64_t rows, int D) {
+  const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
+  const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 4};
+  const cuuint32_t box[2] = {16, 32};
+  const cuuint32_t es[2] = {1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, ptr, dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) ==
+         CUDA_SUCCESS;
+}
+
 bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int D, int box_rows) {
   const cuuint64_t dims[2] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows)};
   const cuuint64_t strides[1] = {static_cast<cuuint64_t>(D) * 2};
@@ -242,7 +255,8 @@ int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, 
   const int step_keys = hp.G * hp.bk;
   if (!encode_map(&prm.tm_q, q, rows, hp.D, wsattn::kTileM) ||
       !encode_map(&prm.tm_k, k, rows, hp.D, step_keys) ||
-      !encode_map(&prm.tm_v, v, rows, hp.D, step_keys))
+      !encode_map(&prm.tm_v, v, rows, hp.D, step_keys) ||
+      !encode_out_map(&prm.tm_o, out, rows, hp.D))
     return WSATTN_ERR_CUDA;
   prm.tiles = plan->d_tiles;
   prm.cls = plan->d_cls;

@@ -89,9 +89,15 @@ enum : int {
 // Exchange area after the barriers: row maxima and row sums of the
 // warpgroups, double-buffered: float [2 parity][kNumWG][128 rows] each.
 constexpr uint32_t kXchBytes = 2 * 2 * kNumWG * 128 * 4;
+// Epilogue staging after the exchange area (128-byte aligned): one 32-row x
+// 16-column fp32 chunk (2 KB) per softmax warp, written row by row and sent
+// to global memory by one TMA store.
+constexpr uint32_t kOChunkBytes = 32 * 16 * 4;
+constexpr uint32_t kOStageBytes = kSoftmaxWarps * kOChunkBytes;
 
 struct Shared {
   uint32_t q, k, v, bars;  // shared-window addresses
+  uint32_t ostage;         // epilogue staging chunks (kOChunkBytes per softmax warp)
   float* xch_m;            // [2][kNumWG][128]
   float* xch_l;            // [2][kNumWG][128]
   volatile int* abort_flag;
@@ -621,12 +627,36 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
     tc_fence_after();
     const float inv = 1.f / lsum;
     float* orow = p.out + grow * D + 16 * og0;
+    // A warp whose 32 rows all belong to the frame stages each 16-column group
+    // in its shared chunk (its rows 64 bytes apart) and sends it with one TMA
+    // store: the per-thread row stores below touch 32 rows per instruction.
+    // Warps of a frame's tail tile store their valid rows themselves.
+    const int wq = warp & 3;
+    const bool warp_full = 32 * wq + 32 <= t.nvalid;
+    const uint32_t chunk = s.ostage + static_cast<uint32_t>(warp - kSoftmaxWarp0) * kOChunkBytes;
+    const int lid = threadIdx.x & 31;
 #pragma unroll 1
     for (int k = 0; k < nog; ++k) {
       uint32_t v[16];
       tmem_ld16(lane + ocol + k * 16, v);
       tmem_wait_ld16(v);
-      if (valid) {
+      if (warp_full) {
+        // the chunk's previous store must have read it
+        if (lid == 0) bulk_wait_read_all();
+        __syncwarp();
+#pragma unroll
+        for (int i = 0; i < 4; ++i)
+          st_shared_v4(chunk + 64u * lid + 16u * i, __float_as_uint(__uint_as_float(v[4 * i]) * inv),
+                       __float_as_uint(__uint_as_float(v[4 * i + 1]) * inv),
+                       __float_as_uint(__uint_as_float(v[4 * i + 2]) * inv),
+                       __float_as_uint(__uint_as_float(v[4 * i + 3]) * inv));
+        fence_proxy_async_smem();
+        __syncwarp();
+        if (lid == 0) {
+          tma_store_2d(&p.tm_o, chunk, 16 * (og0 + k), im.bh * p.n + t.row0 + 32 * wq);
+          bulk_commit_group();
+        }
+      } else if (valid) {
         float4* dst = reinterpret_cast<float4*>(orow + k * 16);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
@@ -656,6 +686,7 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
   uint8_t* gbars = smem_raw + (s.bars - raw);
   s.xch_m = reinterpret_cast<float*>(gbars + 8 * B_COUNT + 16);
   s.xch_l = s.xch_m + 2 * kNumWG * kTileM;
+  s.ostage = (s.bars + 8u * B_COUNT + 16u + kXchBytes + 127u) & ~127u;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(gbars + 8 * B_COUNT);
   s.abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   s.status = p.status;
@@ -705,6 +736,8 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
     if (lane == 0) pv_issuer<D, MAXC>(p, s, tbase);
   } else if (warp >= kSoftmaxWarp0) {
     softmax_wg<D, MAXC>(p, s, tbase);
+    // the epilogue's tile stores must be complete before the CTA exits
+    if (lane == 0) bulk_wait_all();
   }
 
   tc_fence_before();
@@ -765,7 +798,7 @@ cudaError_t launch_d(const FwdParams& p, int grid, size_t smem, cudaStream_t str
 size_t forward_smem_bytes(int D, int step_keys, int stages_k, int stages_v) {
   const size_t stage = static_cast<size_t>(step_keys) * D * 2;
   return 1024 + static_cast<size_t>(kTileM) * D * 2 + (stages_k + stages_v) * stage +
-         8 * B_COUNT + 16 + kXchBytes;
+         8 * B_COUNT + 16 + kXchBytes + 128 + kOStageBytes;
 }
 
 void forward_stages(int D, int step_keys, size_t smem_optin, int* stages_k, int* stages_v) {

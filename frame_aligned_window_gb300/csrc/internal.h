@@ -123,6 +123,7 @@ struct FwdParams {
   CUtensorMap tm_q;  // [BH*N, D] bf16, box {64, 128}, 128-byte swizzle
   CUtensorMap tm_k;  // [BH*N, D] bf16, box {64, G * bk}
   CUtensorMap tm_v;  // [BH*N, D] bf16, box {64, G * bk}
+  CUtensorMap tm_o;  // [BH*N, D] fp32, box {16, 32}, no swizzle (epilogue stores)
   const WorkTile* tiles;
   const int32_t* cls;    // class boundaries into tiles, n_cls + 1 entries
   int n_cls;
