@@ -623,14 +623,17 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
     if (!xch_sync(s, xc)) return;
     float lsum = 0.f;
 #pragma unroll
-    for (int v = 0; v < kNumWG; ++v) lsum += s.xch_l[(lpar * kNumWG + v) * kTileM + r];
+    for (int g = 0; g < kNumWG; ++g) lsum += s.xch_l[(lpar * kNumWG + g) * kTileM + r];
     tc_fence_after();
     const float inv = 1.f / lsum;
     float* orow = p.out + grow * D + 16 * og0;
     // A warp whose 32 rows all belong to the frame stages each 16-column group
     // in its shared chunk (its rows 64 bytes apart) and sends it with one TMA
     // store: the per-thread row stores below touch 32 rows per instruction.
-    // Warps of a frame's tail tile store their valid rows themselves.
+    // The chunk uses the 64-byte swizzle (16-byte unit u of row r sits at unit
+    // u ^ ((r >> 1) & 3)), so each quarter-warp's 16-byte stores fall in eight
+    // different bank groups.  Warps of a frame's tail tile store their valid
+    // rows themselves.
     const int wq = warp & 3;
     const bool warp_full = 32 * wq + 32 <= t.nvalid;
     const uint32_t chunk = s.ostage + static_cast<uint32_t>(warp - kSoftmaxWarp0) * kOChunkBytes;
@@ -646,7 +649,8 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         __syncwarp();
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          st_shared_v4(chunk + 64u * lid + 16u * i, __float_as_uint(__uint_as_float(v[4 * i]) * inv),
+          st_shared_v4(chunk + 64u * lid + 16u * (i ^ ((lid >> 1) & 3)),
+                       __float_as_uint(__uint_as_float(v[4 * i]) * inv),
                        __float_as_uint(__uint_as_float(v[4 * i + 1]) * inv),
                        __float_as_uint(__uint_as_float(v[4 * i + 2]) * inv),
                        __float_as_uint(__uint_as_float(v[4 * i + 3]) * inv));
@@ -686,7 +690,7 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
   uint8_t* gbars = smem_raw + (s.bars - raw);
   s.xch_m = reinterpret_cast<float*>(gbars + 8 * B_COUNT + 16);
   s.xch_l = s.xch_m + 2 * kNumWG * kTileM;
-  s.ostage = (s.bars + 8u * B_COUNT + 16u + kXchBytes + 127u) & ~127u;
+  s.ostage = (s.bars + 8u * B_COUNT + 16u + kXchBytes + 511u) & ~511u;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(gbars + 8 * B_COUNT);
   s.abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   s.status = p.status;
@@ -718,6 +722,7 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
     prefetch_tensormap(&p.tm_q);
     prefetch_tensormap(&p.tm_k);
     prefetch_tensormap(&p.tm_v);
+    prefetch_tensormap(&p.tm_o);
   }
   if (warp == 2) {
     tmem_alloc(smem_u32(tslot), kTmemCols);
@@ -798,7 +803,7 @@ cudaError_t launch_d(const FwdParams& p, int grid, size_t smem, cudaStream_t str
 size_t forward_smem_bytes(int D, int step_keys, int stages_k, int stages_v) {
   const size_t stage = static_cast<size_t>(step_keys) * D * 2;
   return 1024 + static_cast<size_t>(kTileM) * D * 2 + (stages_k + stages_v) * stage +
-         8 * B_COUNT + 16 + kXchBytes + 128 + kOStageBytes;
+         8 * B_COUNT + 16 + kXchBytes + 512 + kOStageBytes;
 }
 
 void forward_stages(int D, int step_keys, size_t smem_optin, int* stages_k, int* stages_v) {
