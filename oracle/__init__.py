@@ -5,8 +5,9 @@ cpu_baseline / reference legs of bench.py may import this package.  It shares
 no code with the CUDA library (frame_aligned_window_gb300) and never imports
 it; the only module both sides use is `workloads` (seeded inputs).
 
-`oracle.c` is plain fp64 C (built here with gcc and OpenMP); `brute.py` is a
-second, pure-Python restatement used to pin the C code on tiny inputs.
+`oracle.c` is plain fp64 C (built here with gcc and OpenMP); `produce` (the
+pre-attention producer) is numpy in fp64 with a library matmul; `brute.py` is
+a second, pure-Python restatement used to pin both on tiny inputs.
 
 Parity status: every function here is pinned by tests under tests/ against
 brute force, closed forms, invariants or a library routine (see the
@@ -194,3 +195,61 @@ def attention_full(q, k, v, F, T, w, R, scale, flags: int = 0) -> np.ndarray:
     nbh, n, d = kd.shape
     pairs = [(h, i) for h in range(nbh) for i in range(n)]
     return attention_rows(q, k, v, F, T, w, R, scale, pairs, flags).reshape(nbh, n, d)
+
+
+def produce(x, w, rope_cos, rope_sin, eps: float, heads: int, head_dim: int, rows=None):
+    """Pre-attention producer, plain definition in fp64 -> (q, k, v).
+
+    Google Developers Blog post "HeyGen x Google Cloud: Bringing Avatar IV to
+    TPUs", section "Layout is ABI" and Figure 5: a chain of small ops
+    (normalisation, rotary embedding, projection, head packing) produces the
+    attention inputs, and one fused kernel writes them straight into the
+    layout the consumer reads.  The pages name the ops only; this oracle takes
+    the plainest reading of each:
+
+      1. RMS normalisation of every token, without a gain (a gain is folded
+         into the projection weights by the caller):
+         xh_t = x_t / sqrt(mean_c x_tc^2 + eps);
+      2. projection without bias: y_t = W xh_t, W [3 H D, C] whose rows are
+         the q features (head-major, dim-minor), then k, then v;
+      3. rotary embedding of q and k: dims (2p, 2p+1) of token t turn by the
+         angle whose cosine and sine are rope_cos[t, p], rope_sin[t, p]
+         ((a, b) -> (a cos - b sin, a sin + b cos)); v is not rotated;
+      4. head packing into [B, H, N, D].
+
+    x: [B, N, C]; w: [3 H D, C]; rope_cos, rope_sin: [N, D / 2] (the table is
+    an input: it encodes the positions).  rows: token indices to compute
+    (default all).  Returns three float64 arrays [B, H, len(rows), D].
+    """
+    xd = np.asarray(x.detach().cpu().to(torch.float64).numpy() if isinstance(x, torch.Tensor)
+                    else x, dtype=np.float64)
+    wd = np.asarray(w.detach().cpu().to(torch.float64).numpy() if isinstance(w, torch.Tensor)
+                    else w, dtype=np.float64)
+    cd = np.asarray(rope_cos.detach().cpu().to(torch.float64).numpy()
+                    if isinstance(rope_cos, torch.Tensor) else rope_cos, dtype=np.float64)
+    sd = np.asarray(rope_sin.detach().cpu().to(torch.float64).numpy()
+                    if isinstance(rope_sin, torch.Tensor) else rope_sin, dtype=np.float64)
+    B, N, C = xd.shape
+    H, D = heads, head_dim
+    if wd.shape != (3 * H * D, C) or cd.shape != (N, D // 2) or sd.shape != (N, D // 2):
+        raise ValueError("produce: shape mismatch")
+    rows = np.arange(N) if rows is None else np.asarray(rows, dtype=np.int64)
+    xs = xd[:, rows, :]                                            # [B, n, C]
+    xh = xs / np.sqrt(np.mean(xs * xs, axis=2, keepdims=True) + eps)
+    y = xh @ wd.T                                                  # [B, n, 3 H D]
+    y = y.reshape(B, len(rows), 3, H, D)
+    c = cd[rows][None, :, None, :]                                 # [1, n, 1, D/2]
+    s = sd[rows][None, :, None, :]
+
+    def rotate(t):
+        a, b = t[..., 0::2], t[..., 1::2]
+        out = np.empty_like(t)
+        out[..., 0::2] = a * c - b * s
+        out[..., 1::2] = a * s + b * c
+        return out
+
+    q = rotate(y[:, :, 0])
+    k = rotate(y[:, :, 1])
+    v = y[:, :, 2]
+    pack = lambda t: np.ascontiguousarray(t.transpose(0, 2, 1, 3))  # noqa: E731
+    return pack(q), pack(k), pack(v)

@@ -4,8 +4,9 @@ TEST INFRASTRUCTURE ONLY (same rule as the rest of oracle/).  A second,
 independent restatement of the definitions in the Google Developers Blog
 post "HeyGen x Google Cloud: Bringing Avatar IV to TPUs" (section "Deleting
 the mask" for the mask, section "Breaking softmax's dependency chain" for the
-bound), written with Python lists, loops and math.exp only, so that the C
-oracle can be checked against it on tiny shapes.
+bound, section "Layout is ABI" for the pre-attention producer), written with
+Python lists, loops and math.exp only, so that the C and numpy oracle can be
+checked against it on tiny shapes.
 """
 from __future__ import annotations
 
@@ -66,3 +67,33 @@ def key_mean(k):
 
 def norm(x):
     return math.sqrt(sum(t * t for t in x))
+
+
+def produce(x, w, rope_cos, rope_sin, eps, heads, head_dim):
+    """Pre-attention producer (section "Layout is ABI" of the same post:
+    normalisation, projection, rotary embedding, head packing), restated with
+    loops on nested lists.  x [B][N][C], w [3HD][C], rope tables [N][D/2].
+    Returns (q, k, v) as nested lists [B][H][N][D]."""
+    B, N, C = len(x), len(x[0]), len(x[0][0])
+    H, D = heads, head_dim
+    result = [[[[[0.0] * D for _ in range(N)] for _ in range(H)] for _ in range(B)]
+              for _ in range(3)]
+    for b in range(B):
+        for t in range(N):
+            ms = sum(val * val for val in x[b][t]) / C
+            inv = 1.0 / math.sqrt(ms + eps)
+            xh = [val * inv for val in x[b][t]]
+            for part in range(3):
+                for h in range(H):
+                    feats = []
+                    for d in range(D):
+                        row = w[part * H * D + h * D + d]
+                        feats.append(sum(row[c] * xh[c] for c in range(C)))
+                    if part < 2:
+                        for p in range(D // 2):
+                            a, bb = feats[2 * p], feats[2 * p + 1]
+                            co, si = rope_cos[t][p], rope_sin[t][p]
+                            feats[2 * p] = a * co - bb * si
+                            feats[2 * p + 1] = a * si + bb * co
+                    result[part][b][h][t] = feats
+    return result[0], result[1], result[2]

@@ -17,6 +17,11 @@ available; these seeded draws stand in for them:
 
 Token order: the R reference frames first, then video frames 0..F-1, each
 T tokens long; tensors are row-major [B, H, N, D] with N = (R + F) * T.
+
+The pre-attention producer takes hidden states x [B, N, C], projection
+weights W [3 H D, C] and a rotary angle table (cos, sin) [N, D / 2]; the
+table is an input that encodes each token's position (frame, row, column of
+the latent grid), built here like any other input (`producer_inputs`).
 """
 from __future__ import annotations
 
@@ -39,6 +44,7 @@ class Workload:
     boost_heads: tuple = ()  # heads whose 1% of query rows are scaled by `boost`
     boost: float = 8.0
     description: str = ""
+    grid_w: int = 0          # columns of a frame's latent grid (0: one row of T)
 
     @property
     def n_tokens(self) -> int:
@@ -56,16 +62,17 @@ class Workload:
 
 
 WORKLOADS = {
-    "tiny": Workload("tiny", 1, 2, 64, 4, 1, 48, 1, 0,
+    "tiny": Workload("tiny", 1, 2, 64, 4, 1, 48, 1, 0, grid_w=8,
                      description="4 frames + 1 reference, 48 tokens/frame"),
-    "small": Workload("small", 1, 8, 128, 9, 1, 208, 1, 1,
+    "small": Workload("small", 1, 8, 128, 9, 1, 208, 1, 1, grid_w=16,
                       description="9 frames + 1 reference, 13x16 tokens/frame"),
-    "sr": Workload("sr", 1, 24, 128, 21, 1, 1040, 2, 2,
+    "sr": Workload("sr", 1, 24, 128, 21, 1, 1040, 2, 2, grid_w=40,
                    description="SR-shaped: 21 frames + 1 reference, 26x40 latent grid"),
     "sr_long": Workload("sr_long", 1, 24, 128, 25, 1, 2080, 3, 3, boost_heads=(5, 17),
+                        grid_w=40,
                         description="SR-long: 25 frames + 1 reference; heads 5 and 17 "
                                     "have 1% of query rows scaled x8"),
-    "dense": Workload("dense", 2, 40, 128, 13, 1, 1568, 12, 4,
+    "dense": Workload("dense", 2, 40, 128, 13, 1, 1568, 12, 4, grid_w=56,
                       description="dense-window A2V-like: 13 frames + 1 reference, 28x56, "
                                   "every frame sees every frame"),
 }
@@ -132,3 +139,46 @@ def micro(seed: int, batch: int, heads: int, head_dim: int, frames: int, ref_fra
     v = torch.randn(shape, generator=g)
     k += off[None, :, None, :]
     return wl, q.to(torch.bfloat16), k.to(torch.bfloat16), v.to(torch.bfloat16)
+
+
+def rope_table(n_tokens: int, tokens_per_frame: int, grid_w: int, head_dim: int,
+               base: float = 10000.0):
+    """Rotary angle table (cos, sin), fp32 [N, D / 2], for tokens laid out as
+    frames of a latent grid grid_w columns wide: the D / 2 dimension pairs are
+    split into a frame group (the remainder), a row group and a column group
+    (floor(D / 6) pairs each); pair j of a group of n pairs turns by
+    position * base^(-j / n)."""
+    half = head_dim // 2
+    n_hw = half // 3
+    n_t = half - 2 * n_hw
+    gw = grid_w if grid_w > 0 else tokens_per_frame
+    tok = torch.arange(n_tokens, dtype=torch.float64)
+    frame = torch.div(tok, tokens_per_frame, rounding_mode="floor")
+    inner = tok - frame * tokens_per_frame
+    row = torch.div(inner, gw, rounding_mode="floor")
+    col = inner - row * gw
+    parts = []
+    for pos, n in ((frame, n_t), (row, n_hw), (col, n_hw)):
+        freq = base ** (-torch.arange(n, dtype=torch.float64) / n)
+        parts.append(pos[:, None] * freq[None, :])
+    ang = torch.cat(parts, dim=1)
+    return torch.cos(ang).to(torch.float32).contiguous(), torch.sin(ang).to(torch.float32).contiguous()
+
+
+def producer_inputs(wl: Workload, model_dim: int = 0, seed_offset: int = 500):
+    """(x, w, rope_cos, rope_sin) for the pre-attention producer of wl.
+
+    C = model_dim or H * D.  Draw order from one torch CPU generator seeded
+    with wl.seed + seed_offset: m [C] (a component every token shares, so the
+    projected keys of a head share one too), z [B, N, C], per-token scales
+    exp(0.5 * N(0, 1)) (so the normalisation matters), W [3 H D, C] / sqrt(C).
+    x = (z + m) * scale, cast to bf16; W cast to bf16."""
+    C = model_dim or wl.heads * wl.head_dim
+    g = torch.Generator().manual_seed(wl.seed + seed_offset)
+    m = torch.randn(C, generator=g)
+    z = torch.randn((wl.batch, wl.n_tokens, C), generator=g)
+    sc = torch.exp(0.5 * torch.randn((wl.batch, wl.n_tokens, 1), generator=g))
+    w = torch.randn((3 * wl.heads * wl.head_dim, C), generator=g) / float(C) ** 0.5
+    x = ((z + m) * sc).to(torch.bfloat16).contiguous()
+    cos, sin = rope_table(wl.n_tokens, wl.tokens_per_frame, wl.grid_w, wl.head_dim)
+    return x, w.to(torch.bfloat16).contiguous(), cos, sin
