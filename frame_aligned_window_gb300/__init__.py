@@ -10,7 +10,7 @@ The names mirror the C ABI:
     wsattn_plan, wsattn_plan_ex, wsattn_plan_destroy, wsattn_prepare, wsattn_forward,
     wsattn_plan_info, wsattn_get_block_map, wsattn_get_csr, wsattn_get_stats,
     wsattn_plan_set_debug, wsattn_plan_set_bound, wsattn_device_status,
-    wsattn_selftest_timeout, wsattn_status_string, wsattn_prepare_static
+    wsattn_selftest_timeout, wsattn_status_string, wsattn_prepare_static, wsattn_produce
 """
 from __future__ import annotations
 
@@ -28,6 +28,7 @@ EXPORTS = (
     "wsattn_plan_info", "wsattn_get_block_map", "wsattn_get_csr", "wsattn_get_stats",
     "wsattn_plan_set_debug", "wsattn_plan_set_bound", "wsattn_device_status",
     "wsattn_selftest_timeout", "wsattn_status_string", "wsattn_prepare_static",
+    "wsattn_produce",
 )
 
 # wsattn_bound
@@ -70,6 +71,7 @@ _lib.wsattn_device_status.argtypes = [_P, _P]
 _lib.wsattn_selftest_timeout.argtypes = [_I, ctypes.POINTER(_I), _P]
 _lib.wsattn_status_string.argtypes = [_I]
 _lib.wsattn_prepare_static.argtypes = [_I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P]
+_lib.wsattn_produce.argtypes = [_P, _I, _P, _I, _P, _P, _P, _F, _P, _P, _P, _P]
 _lib.wsattn_status_string.restype = ctypes.c_char_p
 for _name in EXPORTS:
     if _name != "wsattn_status_string":
@@ -178,6 +180,39 @@ def wsattn_prepare(plan: Plan, q, k, stream=None):
     _check(_lib.wsattn_prepare(plan.handle, q.shape[0], _dev_ptr(q, "q", torch.bfloat16),
                                _dev_ptr(k, "k", torch.bfloat16), _stream_ptr(stream)),
            "wsattn_prepare")
+
+
+def wsattn_produce(plan: Plan, x, w_qkv, rope_cos, rope_sin, eps: float = 1e-6, q=None, k=None,
+                   v=None, stream=None):
+    """Pre-attention producer: x [B, N, C] bf16, w_qkv [3HD, C] bf16, rope
+    tables fp32 [N, D/2] -> (q, k, v) bf16 [B, H, N, D]; the plan's
+    statistics are then ready for wsattn_forward, as after wsattn_prepare."""
+    import torch
+    if x.dim() != 3 or x.shape[1] != plan.n_tokens:
+        raise ValueError(f"x must be [B, {plan.n_tokens}, C], got {tuple(x.shape)}")
+    B, _, C = x.shape
+    hd = plan.heads * plan.head_dim
+    if tuple(w_qkv.shape) != (3 * hd, C):
+        raise ValueError(f"w_qkv must be [{3 * hd}, {C}], got {tuple(w_qkv.shape)}")
+    for t, n in ((rope_cos, "rope_cos"), (rope_sin, "rope_sin")):
+        if tuple(t.shape) != (plan.n_tokens, plan.head_dim // 2):
+            raise ValueError(f"{n} must be [{plan.n_tokens}, {plan.head_dim // 2}]")
+    shape = (B, plan.heads, plan.n_tokens, plan.head_dim)
+    q = torch.empty(shape, dtype=torch.bfloat16, device=x.device) if q is None else q
+    k = torch.empty(shape, dtype=torch.bfloat16, device=x.device) if k is None else k
+    v = torch.empty(shape, dtype=torch.bfloat16, device=x.device) if v is None else v
+    for t, n in ((q, "q"), (k, "k"), (v, "v")):
+        _check_shape(plan, t, n)
+        if t.shape[0] != B:
+            raise ValueError(f"{n} batch differs from x")
+    _check(_lib.wsattn_produce(plan.handle, B, _dev_ptr(x, "x", torch.bfloat16), C,
+                               _dev_ptr(w_qkv, "w_qkv", torch.bfloat16),
+                               _dev_ptr(rope_cos, "rope_cos", torch.float32),
+                               _dev_ptr(rope_sin, "rope_sin", torch.float32), float(eps),
+                               _dev_ptr(q, "q", torch.bfloat16), _dev_ptr(k, "k", torch.bfloat16),
+                               _dev_ptr(v, "v", torch.bfloat16), _stream_ptr(stream)),
+           "wsattn_produce")
+    return q, k, v
 
 
 def wsattn_forward(plan: Plan, q, k, v, out=None, stream=None):

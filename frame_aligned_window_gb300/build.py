@@ -21,7 +21,7 @@ CSRC = os.path.join(HERE, "csrc")
 INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(HERE, "libwsattn.so")
-SOURCES = ["plan.cpp", "prepare.cu", "forward.cu", "api.cu", "prepare_static.cu"]
+SOURCES = ["plan.cpp", "prepare.cu", "forward.cu", "api.cu", "prepare_static.cu", "produce.cu"]
 HEADERS = ["internal.h", "ptx.cuh"]
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]

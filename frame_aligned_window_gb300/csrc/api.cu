@@ -32,6 +32,12 @@ struct wsattn_plan_s {
   int force_path = -1;
   float tau = wsattn::kDefaultTau;
   int bound_mode = WSATTN_BOUND_GLOBAL;
+  // producer workspace (inverse RMS per token, key sums), sized for prod_batch
+  int prod_batch = 0;
+  void* prod_ws = nullptr;
+  float* inv_rms = nullptr;    // [B * N]
+  float* key_parts = nullptr;  // [BH, 4 * ceil(N / 128), D]
+  float* key_sums = nullptr;   // [BH, D]
 };
 
 namespace {
@@ -75,6 +81,37 @@ bool encode_map(CUtensorMap* m, const void* ptr, int64_t rows, int D, int box_ro
   return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
                   box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// x [B, N, C] bf16 as a 3-D map {C, N, B}: 128 tokens x 64 features per
+// box, 128-byte swizzle (K-major tcgen05 operand).  Tokens past N read as
+// zero, so a batch element's last tile never sees the next one's rows.
+bool encode_x_map(CUtensorMap* m, const void* ptr, int B, int64_t N, int C) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(C), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(B)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(C) * 2,
+                                 static_cast<cuuint64_t>(N) * C * 2};
+  const cuuint32_t box[3] = {64, 128, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(ptr), dims, strides,
+                  box, es, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+// q, k or v [BH, N, D] bf16 as a 3-D map {D, N, BH}: 32 tokens x 64
+// dims per box (one epilogue warp's chunk); stores past N are dropped.
+bool encode_head_map(CUtensorMap* m, void* ptr, int BH, int64_t N, int D) {
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(N),
+                              static_cast<cuuint64_t>(BH)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(D) * 2,
+                                 static_cast<cuuint64_t>(N) * D * 2};
+  const cuuint32_t box[3] = {64, 32, 1};
+  const cuuint32_t es[3] = {1, 1, 1};
+  return g_encode(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, ptr, dims, strides, box, es,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_NONE,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
@@ -160,7 +197,38 @@ int ensure_workspace(wsattn_plan_s* p, int batch, cudaStream_t stream) {
   return WSATTN_OK;
 }
 
+// Producer workspace for `batch`; growing it synchronises the stream.
+int ensure_prod_workspace(wsattn_plan_s* p, int batch, cudaStream_t stream) {
+  if (batch <= p->prod_batch) return WSATTN_OK;
+  const HostPlan& hp = p->hp;
+  const size_t BH = static_cast<size_t>(batch) * hp.H;
+  const size_t nparts = 4 * static_cast<size_t>((hp.N + wsattn::kProdTileM - 1) /
+                                                wsattn::kProdTileM);
+  auto up = [](size_t x) { return (x + 255) / 256 * 256; };
+  const size_t n_inv = up(sizeof(float) * batch * hp.N);
+  const size_t n_parts = up(sizeof(float) * BH * nparts * hp.D);
+  const size_t n_sums = up(sizeof(float) * BH * hp.D);
+  if (p->prod_ws) {
+    if (cudaStreamSynchronize(stream) != cudaSuccess) return WSATTN_ERR_CUDA;
+    cudaFree(p->prod_ws);
+    p->prod_ws = nullptr;
+    p->prod_batch = 0;
+  }
+  if (cudaMalloc(&p->prod_ws, n_inv + n_parts + n_sums) != cudaSuccess) {
+    p->prod_ws = nullptr;
+    return WSATTN_ERR_CUDA;
+  }
+  char* c = static_cast<char*>(p->prod_ws);
+  p->inv_rms = reinterpret_cast<float*>(c);
+  p->key_parts = reinterpret_cast<float*>(c + n_inv);
+  p->key_sums = reinterpret_cast<float*>(c + n_inv + n_parts);
+  p->prod_batch = batch;
+  return WSATTN_OK;
+}
+
 void free_device(wsattn_plan_s* p) {
+  if (p->prod_ws) cudaFree(p->prod_ws);
+  p->prod_ws = nullptr;
   if (p->d_tiles) cudaFree(p->d_tiles);
   if (p->d_cls) cudaFree(p->d_cls);
   if (p->d_status) cudaFree(p->d_status);
@@ -169,6 +237,31 @@ void free_device(wsattn_plan_s* p) {
   p->d_cls = nullptr;
   p->d_status = nullptr;
   p->ws = nullptr;
+}
+
+// Enqueues the statistics passes for q, k (global or window bounds); with
+// key_sums ([BH, D], from the producer) the key-sum pass is skipped.
+int enqueue_prepare(wsattn_plan_s* plan, int batch, const void* q, const void* k,
+                    const float* key_sums, cudaStream_t s) {
+  const HostPlan& hp = plan->hp;
+  const int BH = batch * hp.H;
+  int nchunk = 0, rpc = 0;
+  wsattn::FrameWindow win{hp.F + hp.R, hp.F, hp.R, hp.w, hp.flags};
+  const bool window = plan->bound_mode == WSATTN_BOUND_WINDOW;
+  if (window) {
+    nchunk = win.nf;  // one chunk per frame: its maxima are the frame's
+    rpc = hp.T;
+  } else {
+    wsattn::prepare_chunking(BH, hp.N, plan->num_sms, &nchunk, &rpc);
+  }
+  PrepBuffers b = plan->buf;
+  b.nchunk = nchunk;
+  b.rows_per_chunk = rpc;
+  const float scale = 1.0f / std::sqrt(static_cast<float>(hp.D));
+  if (wsattn::launch_prepare(q, k, BH, hp.N, hp.D, scale, plan->tau, b, window ? &win : nullptr,
+                             key_sums, s) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  return WSATTN_OK;
 }
 
 }  // namespace
@@ -213,25 +306,66 @@ int wsattn_prepare(wsattn_plan_t plan, int batch, const void* q, const void* k, 
   if (rc != WSATTN_OK) return rc;
   rc = ensure_workspace(plan, batch, s);
   if (rc != WSATTN_OK) return rc;
+  rc = enqueue_prepare(plan, batch, q, k, nullptr, s);
+  if (rc == WSATTN_OK) plan->prepared_batch = batch;
+  return rc;
+}
+
+int wsattn_produce(wsattn_plan_t plan, int batch, const void* x, int model_dim,
+                   const void* w_qkv, const float* rope_cos, const float* rope_sin, float eps,
+                   void* q, void* k, void* v, void* stream) {
+  if (!plan || batch < 1 || !x || !w_qkv || !rope_cos || !rope_sin || !q || !k || !v)
+    return WSATTN_ERR_BAD_ARG;
+  if (!aligned16(x) || !aligned16(w_qkv) || !aligned16(rope_cos) || !aligned16(rope_sin) ||
+      !aligned16(q) || !aligned16(k) || !aligned16(v))
+    return WSATTN_ERR_BAD_ARG;
+  if (model_dim < wsattn::kProdTileK || model_dim % wsattn::kProdTileK != 0 || !(eps >= 0.f) ||
+      !std::isfinite(eps))
+    return WSATTN_ERR_BAD_ARG;
+  const HostPlan& hp = plan->hp;
+  if (static_cast<int64_t>(batch) * hp.H * hp.N >= (int64_t(1) << 31) ||
+      static_cast<int64_t>(batch) * hp.N * model_dim >= (int64_t(1) << 40))
+    return WSATTN_ERR_BAD_ARG;
+  const int bn = wsattn::produce_tile_n(hp.H, hp.D);
+  if (bn == 0) return WSATTN_ERR_UNSUPPORTED;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int rc = ensure_device(plan);
+  if (rc != WSATTN_OK) return rc;
+  if (wsattn::produce_smem_bytes(bn) > plan->smem_optin) return WSATTN_ERR_UNSUPPORTED;
+  rc = ensure_workspace(plan, batch, s);
+  if (rc != WSATTN_OK) return rc;
+  rc = ensure_prod_workspace(plan, batch, s);
+  if (rc != WSATTN_OK) return rc;
+  if (!get_encode()) return WSATTN_ERR_CUDA;
   const int BH = batch * hp.H;
-  int nchunk = 0, rpc = 0;
-  wsattn::FrameWindow win{hp.F + hp.R, hp.F, hp.R, hp.w, hp.flags};
-  const bool window = plan->bound_mode == WSATTN_BOUND_WINDOW;
-  if (window) {
-    nchunk = win.nf;  // one chunk per frame: its maxima are the frame's
-    rpc = hp.T;
-  } else {
-    wsattn::prepare_chunking(BH, hp.N, plan->num_sms, &nchunk, &rpc);
-  }
-  PrepBuffers b = plan->buf;
-  b.nchunk = nchunk;
-  b.rows_per_chunk = rpc;
-  const float scale = 1.0f / std::sqrt(static_cast<float>(hp.D));
-  if (wsattn::launch_prepare(q, k, BH, hp.N, hp.D, scale, plan->tau, b, window ? &win : nullptr,
-                             s) != cudaSuccess)
+  wsattn::ProdParams prm;
+  std::memset(&prm, 0, sizeof(prm));
+  void* outs[3] = {q, k, v};
+  if (!encode_x_map(&prm.tm_x, x, batch, hp.N, model_dim) ||
+      !encode_map(&prm.tm_w, w_qkv, 3LL * hp.H * hp.D, model_dim, bn))
     return WSATTN_ERR_CUDA;
-  plan->prepared_batch = batch;
-  return WSATTN_OK;
+  for (int i = 0; i < 3; ++i)
+    if (!encode_head_map(&prm.tm_out[i], outs[i], BH, hp.N, hp.D)) return WSATTN_ERR_CUDA;
+  prm.inv_rms = plan->inv_rms;
+  prm.rope_cos = rope_cos;
+  prm.rope_sin = rope_sin;
+  prm.part_sum = plan->key_parts;
+  prm.status = plan->d_status;
+  prm.batch = batch;
+  prm.heads = hp.H;
+  prm.n = static_cast<int>(hp.N);
+  prm.c = model_dim;
+  prm.mtiles = static_cast<int>((hp.N + wsattn::kProdTileM - 1) / wsattn::kProdTileM);
+  prm.ntiles = 3 * hp.H * hp.D / bn;
+  prm.nparts = 4 * prm.mtiles;
+  const int64_t tiles = static_cast<int64_t>(batch) * prm.mtiles * prm.ntiles;
+  const int grid = static_cast<int>(tiles < plan->num_sms ? tiles : plan->num_sms);
+  if (wsattn::launch_produce(prm, static_cast<const uint16_t*>(x), eps, hp.D, bn, grid,
+                             plan->inv_rms, plan->key_sums, s) != cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  rc = enqueue_prepare(plan, batch, q, k, plan->key_sums, s);
+  if (rc == WSATTN_OK) plan->prepared_batch = batch;
+  return rc;
 }
 
 int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, const void* v,

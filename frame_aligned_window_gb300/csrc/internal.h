@@ -110,10 +110,11 @@ struct FrameWindow {
 
 // Enqueues the three prepare passes; returns a cudaError_t.  With `win`
 // non-null the chunks must be the frames and the row bounds use the
-// per-window key-norm maximum.
+// per-window key-norm maximum.  With `key_sums` non-null ([BH, D]: each
+// head's key column sums, from the producer) pass A is skipped.
 cudaError_t launch_prepare(const void* q, const void* k, int BH, int64_t N, int D, float scale,
                            float tau, const PrepBuffers& buf, const FrameWindow* win,
-                           cudaStream_t stream);
+                           const float* key_sums, cudaStream_t stream);
 
 // Chunking of the N rows of one head across CTAs.
 void prepare_chunking(int BH, int64_t N, int num_sms, int* nchunk, int* rows_per_chunk);
@@ -147,6 +148,33 @@ size_t forward_smem_bytes(int D, int step_keys, int stages_k, int stages_v);
 void forward_stages(int D, int step_keys, size_t smem_optin, int* stages_k, int* stages_v);
 // Launches the persistent forward kernel on `grid` CTAs.
 cudaError_t launch_forward(const FwdParams& p, int D, int grid, size_t smem, cudaStream_t s);
+
+// ------------------------------------------------------------ producer
+// Pre-attention producer: y = (x W^T) / rms(x), rotary turn of q and k,
+// bf16, head-packed [B, H, N, D] stores, and per-32-row key column sums.
+constexpr int kProdTileM = 128;  // tokens per tile (one batch element)
+constexpr int kProdTileK = 64;   // model-dim slice per pipeline stage
+struct ProdParams {
+  CUtensorMap tm_x;       // x [B, N, C] bf16, 3-D {C, N, B}, box {64, 128, 1}, 128-byte swizzle
+  CUtensorMap tm_w;       // W [3HD, C] bf16, 2-D, box {64, BN}, 128-byte swizzle
+  CUtensorMap tm_out[3];  // q, k, v [BH, N, D] bf16, 3-D {D, N, BH}, box {64, 32, 1}, swizzled
+  const float* inv_rms;   // [B * N] 1 / sqrt(mean x^2 + eps)
+  const float* rope_cos;  // [N, D / 2]
+  const float* rope_sin;  // [N, D / 2]
+  float* part_sum;        // [BH, nparts, D] key column sums of 32-row groups
+  int* status;            // device status word (bit set on an expired wait)
+  int batch, heads, n, c;
+  int mtiles;             // ceil(N / 128)
+  int ntiles;             // 3HD / BN
+  int nparts;             // 4 * mtiles
+};
+// BN (feature columns per tile) for H * D, 0 if unsupported.
+int produce_tile_n(int heads, int head_dim);
+size_t produce_smem_bytes(int bn);
+// RMS pre-pass, the producer GEMM and the reduction of the key column sums
+// into [BH, D]; returns a cudaError_t.
+cudaError_t launch_produce(const ProdParams& p, const uint16_t* x, float eps, int D, int bn,
+                           int grid, float* inv_rms, float* key_sums, cudaStream_t stream);
 
 // Self test of the bounded wait (see wsattn_selftest_timeout).
 cudaError_t launch_timeout_selftest(long long limit_cycles, int* status, cudaStream_t s);

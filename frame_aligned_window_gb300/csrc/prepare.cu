@@ -112,7 +112,7 @@ __global__ void __launch_bounds__(kPrepThreads)
 template <int D>
 __global__ void __launch_bounds__(kPrepThreads)
     prep_pass_b(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k, int64_t n, int rpc,
-                int nchunk, float scale, const float* __restrict__ part_sum,
+                int nchunk, float scale, const float* __restrict__ part_sum, int nsum,
                 float* __restrict__ mu_out, float* __restrict__ qn, float* __restrict__ crow,
                 float* __restrict__ part_kmax, float* __restrict__ part_qmax) {
   constexpr int kLanes = D / 8;
@@ -123,8 +123,8 @@ __global__ void __launch_bounds__(kPrepThreads)
   const int lr = threadIdx.x % kLanes, rs = threadIdx.x / kLanes;
   if (threadIdx.x < D) {
     float s = 0.f;
-    for (int cc = 0; cc < nchunk; ++cc)
-      s += part_sum[(static_cast<size_t>(bh) * nchunk + cc) * D + threadIdx.x];
+    for (int cc = 0; cc < nsum; ++cc)
+      s += part_sum[(static_cast<size_t>(bh) * nsum + cc) * D + threadIdx.x];
     const float m = s / static_cast<float>(n);
     mu_s[threadIdx.x] = m;
     if (c == 0) mu_out[static_cast<size_t>(bh) * D + threadIdx.x] = m;
@@ -286,21 +286,26 @@ void prepare_chunking(int BH, int64_t N, int num_sms, int* nchunk, int* rows_per
 
 cudaError_t launch_prepare(const void* q, const void* k, int BH, int64_t N, int D, float scale,
                            float tau, const PrepBuffers& b, const FrameWindow* win,
-                           cudaStream_t stream) {
+                           const float* key_sums, cudaStream_t stream) {
   const dim3 grid(b.nchunk, BH);
   const uint16_t* q16 = static_cast<const uint16_t*>(q);
   const uint16_t* k16 = static_cast<const uint16_t*>(k);
+  // key column sums: pass A's per-chunk sums, or one row per head given
+  const float* sums = key_sums ? key_sums : b.part_sum;
+  const int nsum = key_sums ? 1 : b.nchunk;
   if (D == 128) {
-    prep_pass_a<128><<<grid, kPrepThreads, 0, stream>>>(k16, N, b.rows_per_chunk, b.nchunk,
-                                                        b.part_sum);
+    if (!key_sums)
+      prep_pass_a<128><<<grid, kPrepThreads, 0, stream>>>(k16, N, b.rows_per_chunk, b.nchunk,
+                                                          b.part_sum);
     prep_pass_b<128><<<grid, kPrepThreads, 0, stream>>>(
-        q16, k16, N, b.rows_per_chunk, b.nchunk, scale, b.part_sum, b.mu, b.b_rows, b.m_rows,
+        q16, k16, N, b.rows_per_chunk, b.nchunk, scale, sums, nsum, b.mu, b.b_rows, b.m_rows,
         b.part_kmax, b.part_qmax);
   } else {
-    prep_pass_a<64><<<grid, kPrepThreads, 0, stream>>>(k16, N, b.rows_per_chunk, b.nchunk,
-                                                       b.part_sum);
+    if (!key_sums)
+      prep_pass_a<64><<<grid, kPrepThreads, 0, stream>>>(k16, N, b.rows_per_chunk, b.nchunk,
+                                                         b.part_sum);
     prep_pass_b<64><<<grid, kPrepThreads, 0, stream>>>(
-        q16, k16, N, b.rows_per_chunk, b.nchunk, scale, b.part_sum, b.mu, b.b_rows, b.m_rows,
+        q16, k16, N, b.rows_per_chunk, b.nchunk, scale, sums, nsum, b.mu, b.b_rows, b.m_rows,
         b.part_kmax, b.part_qmax);
   }
   if (win)

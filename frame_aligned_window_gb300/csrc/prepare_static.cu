@@ -121,7 +121,7 @@ extern "C" int wsattn_prepare_static(int batch, int heads, int n_tokens, int hea
   b.nchunk = nchunk;
   b.rows_per_chunk = rpc;
   const float scale = 1.0f / sqrtf(static_cast<float>(head_dim));
-  if (launch_prepare(q, k, BH, N, head_dim, scale, tau, b, nullptr,
+  if (launch_prepare(q, k, BH, N, head_dim, scale, tau, b, nullptr, nullptr,
                      static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return WSATTN_ERR_CUDA;

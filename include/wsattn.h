@@ -130,6 +130,43 @@ int wsattn_plan_destroy(wsattn_plan_t plan);
 int wsattn_prepare(wsattn_plan_t plan, int batch, const void* q, const void* k, void* stream);
 
 /*
+ * Pre-attention producer with the statistics folded in (Google Developers
+ * Blog post "HeyGen x Google Cloud: Bringing Avatar IV to TPUs", section
+ * "Layout is ABI", Figure 5: normalisation, rotary embedding, projection and
+ * head packing fused into one kernel that writes the attention's input
+ * layout).  The pages name the ops only; this call takes, per token t of
+ * every batch element:
+ *   xh_t = x_t / sqrt(mean_c x_tc^2 + eps)   RMS normalisation, no gain (fold
+ *                                           a gain into w_qkv's columns)
+ *   y_t  = w_qkv xh_t                       projection, no bias; y_t holds
+ *                                           the q features (head-major,
+ *                                           dim-minor), then k, then v
+ *   q, k: dims (2p, 2p+1) turn by the angle whose cosine and sine are
+ *         rope_cos[t][p], rope_sin[t][p]: (a, b) -> (a c - b s, a s + b c);
+ *         v is not turned
+ *   q, k, v rounded to bf16 and written [batch, H, N, D]
+ * and then computes the fixed-max statistics of wsattn_prepare for the q and
+ * k it wrote (the key mean from column sums the projection kernel emits, so
+ * k is not read back for it).  After it, wsattn_forward may run on q, k, v
+ * with the same batch, as after wsattn_prepare.  The product W x_t runs on
+ * the tensor cores in fp32; 1 / rms_t is applied to its fp32 result.
+ *   x          bf16 [batch, N, model_dim]
+ *   model_dim  C, a multiple of 64
+ *   w_qkv      bf16 [3 * H * D, model_dim], row-major
+ *   rope_cos   fp32 [N, D / 2] (the angle table: it encodes each token's
+ *   rope_sin   fp32 [N, D / 2]  position; shared by the batch and the heads)
+ *   eps        >= 0
+ *   q, k, v    bf16 [batch, H, N, D] outputs, fully overwritten
+ * Needs H * D to be a multiple of 128.  All pointers 16-byte aligned device
+ * memory; x, w_qkv and the tables are read only.  The plan's workspace grows
+ * as for wsattn_prepare.
+ * Errors: BAD_ARG, UNSUPPORTED (H * D not a multiple of 128), CUDA.
+ */
+int wsattn_produce(wsattn_plan_t plan, int batch, const void* x, int model_dim,
+                   const void* w_qkv, const float* rope_cos, const float* rope_sin, float eps,
+                   void* q, void* k, void* v, void* stream);
+
+/*
  * out = masked softmax(q k^T * scale) v, computed in one pass over the
  * plan's active key blocks by a persistent tcgen05 kernel: QK^T and PV on
  * the tensor cores (bf16 inputs, fp32 accumulation in tensor memory), the
