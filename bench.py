@@ -1,7 +1,7 @@
 """Benchmark of the frame-aligned window-sparse attention hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl wsattn|reference]
-                    [--workload sr] [--block-k 0] [--no-cpu-baseline]
+                    [--workload sr] [--block-k 0] [--no-cpu-baseline] [--produce-steps 20]
 
 A step is one pass of the whole hot path over one batch of synthetic input:
 wsattn_prepare (key mean, row bounds, eligibility) + wsattn_forward (fused
@@ -11,6 +11,11 @@ plan (block map) is built once per shape, outside the timed region.
 Metric: effective TFLOP/s on active blocks = 4 * D * (active query-key pairs)
 * B * H per step / step time.  Inputs (q, k, v 140 MB each, out 281 MB at the
 SR shape) are larger than L2, so no flush runs between steps.
+
+After the timed steps, `--produce-steps` calls of wsattn_produce (the
+pre-attention producer: RMS scale, QKV projection, rotary turn, head packing
+and the statistics) are timed on their own and reported under "produce",
+against the bf16 tensor peak (2 * B * N * C * 3HD FLOP per call, C = H * D).
 
 Under torchrun every rank runs its own replica of the workload (the path has
 no exchange step); value = work of all ranks / the slowest rank's time.
@@ -354,6 +359,35 @@ def run_gpu(args, wl, world, rank, local):
     torch.cuda.synchronize()
     _barrier(world)
     e2e_ms = max_over_ranks(e_begin.elapsed_time(e_end) / e2e_steps, world)
+
+    # The pre-attention producer (x -> q, k, v plus the statistics), timed on
+    # its own: one wsattn_produce call per iteration, inputs resident in HBM.
+    prod = None
+    if args.produce_steps > 0 and (wl.heads * wl.head_dim) % 128 == 0:
+        from workloads import producer_inputs
+        x, w, rc_, rs_ = (t.to(dev) for t in producer_inputs(wl))
+        pq, pk, pv = (torch.empty_like(qd) for _ in range(3))
+        for _ in range(3):
+            fw.wsattn_produce(plan, x, w, rc_, rs_, 1e-6, pq, pk, pv)
+        torch.cuda.synchronize()
+        pe = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+              for _ in range(args.produce_steps)]
+        for a, b in pe:
+            a.record(stream)
+            fw.wsattn_produce(plan, x, w, rc_, rs_, 1e-6, pq, pk, pv)
+            b.record(stream)
+        torch.cuda.synchronize()
+        if fw.wsattn_device_status(plan) != 0:
+            raise RuntimeError("device status after wsattn_produce")
+        p_ms = statistics.mean(a.elapsed_time(b) for a, b in pe)
+        C = x.shape[2]
+        p_flops = 2.0 * wl.batch * wl.n_tokens * C * 3 * wl.heads * wl.head_dim
+        prod = {"ms_per_call": p_ms, "calls": args.produce_steps, "model_dim": C,
+                "gflop_per_call": p_flops / 1e9, "launches": 5,
+                "includes": "RMS pre-pass, projection GEMM, key-sum reduction and the two "
+                            "statistics passes",
+                "achieved_tflops": p_flops / (p_ms * 1e-3) / 1e12}
+        del x, w, rc_, rs_, pq, pk, pv
     if clocks:
         clocks.stop()
 
@@ -402,6 +436,9 @@ def run_gpu(args, wl, world, rank, local):
                 "d2h_bytes_per_step": elem * 4,
                 "copies": "pinned host <-> device on two copy streams, overlapping the "
                           "compute of the neighbouring steps (double-buffered device side)"},
+        "produce": None if prod is None else dict(
+            prod, bound="tensor", peak=peaks["bf16_tflops"], unit="TFLOP/s",
+            frac=prod["achieved_tflops"] / peaks["bf16_tflops"]),
         "gpu_launches": 4 * args.steps,
         "clocks": clocks.summary() if clocks else None,
     }
@@ -417,6 +454,8 @@ def main():
     ap.add_argument("--workload", default="sr")
     ap.add_argument("--block-k", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--produce-steps", type=int, default=20,
+                    help="wsattn_produce calls timed after the attention steps (0: none)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for the cpu_baseline sample")
     args = ap.parse_args()

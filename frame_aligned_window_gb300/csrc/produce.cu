@@ -367,28 +367,36 @@ __global__ void __launch_bounds__(256) rms_kernel(const uint16_t* __restrict__ x
 }
 
 // Key column sums per head: the ordered sum of the epilogue's 32-row group
-// sums.  Thread (g, d) sums groups g, g + 4, ... with eight interleaved
-// accumulators (independent loads in flight), then the accumulators and the
-// four thread groups combine in a fixed order.
-template <int D>
-__global__ void __launch_bounds__(D * 4) reduce_key_sums(const float* __restrict__ parts,
-                                                         int nparts, float* __restrict__ out) {
-  __shared__ float red[4][D];
-  const int bh = blockIdx.x, d = threadIdx.x % D, g = threadIdx.x / D;
-  const float* src = parts + static_cast<size_t>(bh) * nparts * D + d;
+// sums.  A CTA takes 32 columns of one head; thread (g, c) sums groups g,
+// g + 16, ... into eight interleaved accumulators (independent loads in
+// flight), then the accumulators and the 16 thread rows combine in a fixed
+// order.
+constexpr int kRedRows = 16;
+__global__ void __launch_bounds__(32 * kRedRows) reduce_key_sums(const float* __restrict__ parts,
+                                                                 int nparts, int D,
+                                                                 float* __restrict__ out) {
+  __shared__ float red[kRedRows][32];
+  const int bh = blockIdx.y, c = 32 * blockIdx.x + threadIdx.x, g = threadIdx.y;
+  const float* src = parts + static_cast<size_t>(bh) * nparts * D + c;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
   int i = g;
-  for (; i + 28 < nparts; i += 32) {
+  for (; i + 7 * kRedRows < nparts; i += 8 * kRedRows) {
 #pragma unroll
-    for (int u = 0; u < 8; ++u) acc[u] += src[static_cast<size_t>(i + 4 * u) * D];
+    for (int u = 0; u < 8; ++u) acc[u] += src[static_cast<size_t>(i + kRedRows * u) * D];
   }
-  for (int u = 0; i < nparts; i += 4, ++u) acc[u & 7] += src[static_cast<size_t>(i) * D];
+#pragma unroll
+  for (int u = 0; u < 8; ++u)
+    if (i + kRedRows * u < nparts) acc[u] += src[static_cast<size_t>(i + kRedRows * u) * D];
   float sum = 0.f;
 #pragma unroll
   for (int u = 0; u < 8; ++u) sum += acc[u];
-  red[g][d] = sum;
+  red[g][threadIdx.x] = sum;
   __syncthreads();
-  if (g == 0) out[static_cast<size_t>(bh) * D + d] = ((red[0][d] + red[1][d]) + red[2][d]) + red[3][d];
+  if (g == 0) {
+    float t = 0.f;
+    for (int r = 0; r < kRedRows; ++r) t += red[r][threadIdx.x];
+    out[static_cast<size_t>(bh) * D + c] = t;
+  }
 }
 
 template <int D, int BN>
@@ -432,10 +440,8 @@ cudaError_t launch_produce(const ProdParams& p, const uint16_t* x, float eps, in
     e = bn == 256 ? launch_gemm<64, 256>(p, grid, stream) : launch_gemm<64, 128>(p, grid, stream);
   if (e != cudaSuccess) return e;
   const int BH = p.batch * p.heads;
-  if (D == 128)
-    reduce_key_sums<128><<<BH, 128 * 4, 0, stream>>>(p.part_sum, p.nparts, key_sums);
-  else
-    reduce_key_sums<64><<<BH, 64 * 4, 0, stream>>>(p.part_sum, p.nparts, key_sums);
+  reduce_key_sums<<<dim3(D / 32, BH), dim3(32, kRedRows), 0, stream>>>(p.part_sum, p.nparts, D,
+                                                                      key_sums);
   return cudaGetLastError();
 }
 

@@ -91,7 +91,15 @@ def test_produce_statistics_match_prepare_and_oracle():
     np.testing.assert_array_equal(st["elig"], st2["elig"])
     for key in ("mu", "kmax", "b", "m", "bmax"):
         np.testing.assert_allclose(st[key], st2[key], rtol=1e-5, atol=1e-6)
-    np.testing.assert_allclose(out_p.cpu().numpy(), out2.cpu().numpy(), rtol=0, atol=1e-5)
+    # The two row maxima m_i differ by fp32 rounding only (the key mean is
+    # summed in another order), but P = bf16(2^(s - m)) can round the other
+    # way: each P_ij then moves by at most 2^-8 of itself, and out_i (a
+    # P-weighted mean of the v_j, P and l from the same P) by at most
+    # 2 * 2^-8 * max |v_j|.  Such flips are rare, so the relative L2
+    # difference stays far smaller.
+    a, b2 = out_p.cpu().double().numpy(), out2.cpu().double().numpy()
+    assert np.abs(a - b2).max() <= 2.0 ** -7 * float(v.float().abs().max())
+    assert rel_l2(a, b2) <= 1e-4
     # against the oracle's statistics of its own outputs rounded to bf16
     qo, ko, _ = oracle.produce(x, w, c, s, EPS, wl.heads, wl.head_dim)
     qb = torch.from_numpy(qo).to(torch.bfloat16)
