@@ -342,7 +342,7 @@ int wsattn_produce(wsattn_plan_t plan, int batch, const void* x, int model_dim,
   std::memset(&prm, 0, sizeof(prm));
   void* outs[3] = {q, k, v};
   if (!encode_x_map(&prm.tm_x, x, batch, hp.N, model_dim) ||
-      !encode_map(&prm.tm_w, w_qkv, 3LL * hp.H * hp.D, model_dim, bn))
+      !encode_map(&prm.tm_w, w_qkv, 3LL * hp.H * hp.D, model_dim, bn / 2))
     return WSATTN_ERR_CUDA;
   for (int i = 0; i < 3; ++i)
     if (!encode_head_map(&prm.tm_out[i], outs[i], BH, hp.N, hp.D)) return WSATTN_ERR_CUDA;
@@ -357,9 +357,9 @@ int wsattn_produce(wsattn_plan_t plan, int batch, const void* x, int model_dim,
   prm.c = model_dim;
   prm.mtiles = static_cast<int>((hp.N + wsattn::kProdTileM - 1) / wsattn::kProdTileM);
   prm.ntiles = 3 * hp.H * hp.D / bn;
+  prm.mpairs = (prm.mtiles + 1) / 2;
   prm.nparts = 4 * prm.mtiles;
-  const int64_t tiles = static_cast<int64_t>(batch) * prm.mtiles * prm.ntiles;
-  const int grid = static_cast<int>(tiles < plan->num_sms ? tiles : plan->num_sms);
+  const int grid = plan->num_sms;  // an upper bound: the launch sizes the cluster grid
   if (wsattn::launch_produce(prm, static_cast<const uint16_t*>(x), eps, hp.D, bn, grid,
                              plan->inv_rms, plan->key_sums, s) != cudaSuccess)
     return WSATTN_ERR_CUDA;

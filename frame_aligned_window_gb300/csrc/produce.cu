@@ -23,8 +23,12 @@
 // Kernel shape (one CTA per SM, persistent): tiles of 128 tokens x BN
 // features (BN = 256, or 128 when H * D is not a multiple of 256), 64-wide
 // model-dim stages in a 4-deep TMA ring, two TMEM accumulators so the MMA of
-// one tile overlaps the epilogue of the previous one.
-//   warp 0  TMA producer (x tile 128 x 64, W tile BN x 64 per stage)
+// one tile overlaps the epilogue of the previous one.  CTAs run in clusters
+// of two that take the two token tiles of one feature tile: each CTA loads
+// its own x tile and half of the W tile, multicast into both CTAs, so a
+// stage costs 32 KB of L2 traffic per CTA instead of 48 KB (a stage slot is
+// refilled only when both CTAs' MMAs have released it).
+//   warp 0  TMA producer (x tile 128 x 64, half the W tile BN/2 x 64)
 //   warp 1  MMA issuer: 4 x tcgen05.mma M=128 N=BN K=16 per stage
 //   warp 2  TMEM allocation
 //   warps 4-7 epilogue: thread = token row (TMEM lane)
@@ -87,29 +91,36 @@ struct PTile {
   int b, mt, nt;
 };
 
-__device__ __forceinline__ PTile decode(const ProdParams& p, int t) {
+// Work unit t of a cluster: feature tile nt of token tiles 2 mp and 2 mp + 1
+// of batch element b; this CTA takes token tile 2 mp + rank (which is past
+// the last tile when mtiles is odd: its rows read as zero and store nothing).
+__device__ __forceinline__ PTile decode(const ProdParams& p, int t, uint32_t rank) {
   PTile r;
   r.nt = t % p.ntiles;
   const int rest = t / p.ntiles;
-  r.mt = rest % p.mtiles;
-  r.b = rest / p.mtiles;
+  r.mt = 2 * (rest % p.mpairs) + static_cast<int>(rank);
+  r.b = rest / p.mpairs;
   return r;
 }
 
 template <int BN>
-__device__ void p_producer(const ProdParams& p, const PShared& s, int total) {
+__device__ void p_producer(const ProdParams& p, const PShared& s, int total, uint32_t rank,
+                           int cl, int ncl) {
   constexpr uint32_t kStage = kPABytes + BN * kProdTileK * 2;
+  constexpr uint32_t kHalfB = BN / 2 * kProdTileK * 2;
   const int ksteps = p.c / kProdTileK;
   uint32_t slot = 0, phase = 0;
-  for (int t = blockIdx.x; t < total; t += gridDim.x) {
-    const PTile tl = decode(p, t);
+  for (int t = cl; t < total; t += ncl) {
+    const PTile tl = decode(p, t, rank);
     for (int kt = 0; kt < ksteps; ++kt) {
+      // both CTAs' MMAs have released the slot: the peer's half may land too
       if (!pwait(s, pbar(s, PB_EMPTY0 + slot), phase ^ 1u, kStatusTimeoutProducer)) return;
       const uint32_t dst = s.stages + slot * kStage;
-      mbar_arrive_expect_tx(pbar(s, PB_FULL0 + slot), kStage);
+      mbar_arrive_expect_tx(pbar(s, PB_FULL0 + slot), kStage);  // own x, both W halves
       tma_load_3d(dst, &p.tm_x, pbar(s, PB_FULL0 + slot), kt * kProdTileK, tl.mt * kProdTileM,
                   tl.b);
-      tma_load_2d(dst + kPABytes, &p.tm_w, pbar(s, PB_FULL0 + slot), kt * kProdTileK, tl.nt * BN);
+      tma_load_2d_mc(dst + kPABytes + rank * kHalfB, &p.tm_w, pbar(s, PB_FULL0 + slot),
+                     kt * kProdTileK, tl.nt * BN + static_cast<int>(rank) * (BN / 2), 0x3);
       if (++slot == kPStages) {
         slot = 0;
         phase ^= 1u;
@@ -119,12 +130,13 @@ __device__ void p_producer(const ProdParams& p, const PShared& s, int total) {
 }
 
 template <int BN>
-__device__ void p_mma(const ProdParams& p, const PShared& s, int total, uint32_t tbase) {
+__device__ void p_mma(const ProdParams& p, const PShared& s, int total, uint32_t tbase, int cl,
+                      int ncl) {
   constexpr uint32_t kStage = kPABytes + BN * kProdTileK * 2;
   constexpr uint32_t idesc = idesc_bf16_f32(kProdTileM, BN, false);
   const int ksteps = p.c / kProdTileK;
   uint32_t slot = 0, phase = 0, it = 0;
-  for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
+  for (int t = cl; t < total; t += ncl, ++it) {
     const uint32_t ab = it & 1u, use = it >> 1;
     if (!pwait(s, pbar(s, PB_ACCEMPTY0 + ab), (use & 1u) ^ 1u, kStatusTimeoutMma)) return;
     tc_fence_after();
@@ -139,7 +151,7 @@ __device__ void p_mma(const ProdParams& p, const PShared& s, int total, uint32_t
 #pragma unroll
       for (int kk = 0; kk < kProdTileK / 16; ++kk)
         mma_ss(d, ad + 2 * kk, bd + 2 * kk, idesc, (kt | kk) != 0 ? 1u : 0u);
-      tc_commit(pbar(s, PB_EMPTY0 + slot));
+      tc_commit_mc(pbar(s, PB_EMPTY0 + slot), 0x3);  // release the slot in both CTAs
       if (++slot == kPStages) {
         slot = 0;
         phase ^= 1u;
@@ -193,15 +205,16 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
 }
 
 template <int D, int BN>
-__device__ void p_epilogue(const ProdParams& p, const PShared& s, int total, uint32_t tbase) {
+__device__ void p_epilogue(const ProdParams& p, const PShared& s, int total, uint32_t tbase,
+                           uint32_t rank, int cl, int ncl) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int wq = warp - kPEpiWarp0;  // TMEM lanes 32 wq .. 32 wq + 31
   const int r = 32 * wq + lane;
   const uint32_t tlane = tbase + (static_cast<uint32_t>(32 * wq) << 16);
   const int hd = p.heads * D;
   uint32_t it = 0, ob = 0;
-  for (int t = blockIdx.x; t < total; t += gridDim.x, ++it) {
-    const PTile tl = decode(p, t);
+  for (int t = cl; t < total; t += ncl, ++it) {
+    const PTile tl = decode(p, t, rank);
     const uint32_t ab = it & 1u, use = it >> 1;
     const bool ok = pwait(s, pbar(s, PB_ACCFULL0 + ab), use & 1u, kStatusTimeoutSoftmax);
     if (!__all_sync(0xffffffffu, ok)) return;
@@ -248,7 +261,7 @@ __device__ void p_epilogue(const ProdParams& p, const PShared& s, int total, uin
       uint32_t pk[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) pk[i] = bf16x2(y[2 * i], y[2 * i + 1]);
-      if (kind == 1) {
+      if (kind == 1 && tl.mt < p.mtiles) {
         // sums of the stored (rounded) keys; rows past N hold zeros
         float a[64];
 #pragma unroll
@@ -297,12 +310,14 @@ __global__ void __launch_bounds__(kPThreads, 1) produce_kernel(const __grid_cons
   s.abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   s.status = p.status;
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-  const int total = p.batch * p.mtiles * p.ntiles;
+  const int total = p.batch * p.mpairs * p.ntiles;  // work units of a cluster
+  const uint32_t rank = cluster_ctarank();
+  const int cl = static_cast<int>(blockIdx.x / 2), ncl = static_cast<int>(gridDim.x / 2);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPStages; ++i) {
       mbar_init(pbar(s, PB_FULL0 + i), 1);
-      mbar_init(pbar(s, PB_EMPTY0 + i), 1);
+      mbar_init(pbar(s, PB_EMPTY0 + i), 2);  // both CTAs' MMAs release a slot
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(pbar(s, PB_ACCFULL0 + i), 1);
@@ -322,20 +337,22 @@ __global__ void __launch_bounds__(kPThreads, 1) produce_kernel(const __grid_cons
   }
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // the peer's barriers are initialised before any multicast reaches them
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
   if (warp == 0) {
-    if (lane == 0) p_producer<BN>(p, s, total);
+    if (lane == 0) p_producer<BN>(p, s, total, rank, cl, ncl);
   } else if (warp == 1) {
-    if (lane == 0) p_mma<BN>(p, s, total, tbase);
+    if (lane == 0) p_mma<BN>(p, s, total, tbase, cl, ncl);
   } else if (warp >= kPEpiWarp0) {
-    p_epilogue<D, BN>(p, s, total, tbase);
+    p_epilogue<D, BN>(p, s, total, tbase, rank, cl, ncl);
     if (lane == 0) bulk_wait_all();  // the tile stores must be complete before the CTA exits
   }
 
   tc_fence_before();
   __syncthreads();
+  cluster_sync();  // no CTA leaves while its peer may still signal its barriers
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tbase, 2 * BN);
 }
@@ -399,18 +416,41 @@ __global__ void __launch_bounds__(32 * kRedRows) reduce_key_sums(const float* __
   }
 }
 
+// Clusters of two CTAs, as many as can be resident at once (a persistent
+// grid: clusters beyond that would wait for a second wave).
 template <int D, int BN>
-cudaError_t launch_gemm(const ProdParams& p, int grid, cudaStream_t stream) {
+cudaError_t launch_gemm(const ProdParams& p, int max_ctas, cudaStream_t stream) {
   static bool attr_set = false;
+  static int max_clusters = 0;
+  const size_t smem = produce_smem_bytes(BN);
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kPThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   if (!attr_set) {
-    const cudaError_t e = cudaFuncSetAttribute(produce_kernel<D, BN>,
-                                               cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                               static_cast<int>(produce_smem_bytes(BN)));
+    cudaError_t e = cudaFuncSetAttribute(produce_kernel<D, BN>,
+                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         static_cast<int>(smem));
     if (e != cudaSuccess) return e;
+    cfg.gridDim = dim3(2);
+    e = cudaOccupancyMaxActiveClusters(&max_clusters, produce_kernel<D, BN>, &cfg);
+    if (e != cudaSuccess) return e;
+    if (max_clusters < 1) return cudaErrorInvalidConfiguration;
     attr_set = true;
   }
-  produce_kernel<D, BN><<<grid, kPThreads, produce_smem_bytes(BN), stream>>>(p);
-  return cudaGetLastError();
+  const int units = p.batch * p.mpairs * p.ntiles;
+  int clusters = max_ctas / 2 < max_clusters ? max_ctas / 2 : max_clusters;
+  if (clusters > units) clusters = units;
+  if (clusters < 1) clusters = 1;
+  cfg.gridDim = dim3(2 * clusters);
+  return cudaLaunchKernelEx(&cfg, produce_kernel<D, BN>, p);
 }
 
 }  // namespace
