@@ -109,6 +109,8 @@ __device__ void p_producer(const ProdParams& p, const PShared& s, int total, uin
   constexpr uint32_t kStage = kPABytes + BN * kProdTileK * 2;
   constexpr uint32_t kHalfB = BN / 2 * kProdTileK * 2;
   const int ksteps = p.c / kProdTileK;
+  // W is re-read for every token tile: keep it in L2 ahead of the streams
+  const uint64_t keep = policy_evict_last();
   uint32_t slot = 0, phase = 0;
   for (int t = cl; t < total; t += ncl) {
     const PTile tl = decode(p, t, rank);
@@ -119,8 +121,9 @@ __device__ void p_producer(const ProdParams& p, const PShared& s, int total, uin
       mbar_arrive_expect_tx(pbar(s, PB_FULL0 + slot), kStage);  // own x, both W halves
       tma_load_3d(dst, &p.tm_x, pbar(s, PB_FULL0 + slot), kt * kProdTileK, tl.mt * kProdTileM,
                   tl.b);
-      tma_load_2d_mc(dst + kPABytes + rank * kHalfB, &p.tm_w, pbar(s, PB_FULL0 + slot),
-                     kt * kProdTileK, tl.nt * BN + static_cast<int>(rank) * (BN / 2), 0x3);
+      tma_load_2d_mc_hint(dst + kPABytes + rank * kHalfB, &p.tm_w, pbar(s, PB_FULL0 + slot),
+                          kt * kProdTileK, tl.nt * BN + static_cast<int>(rank) * (BN / 2), 0x3,
+                          keep);
       if (++slot == kPStages) {
         slot = 0;
         phase ^= 1u;
@@ -212,6 +215,7 @@ __device__ void p_epilogue(const ProdParams& p, const PShared& s, int total, uin
   const int r = 32 * wq + lane;
   const uint32_t tlane = tbase + (static_cast<uint32_t>(32 * wq) << 16);
   const int hd = p.heads * D;
+  const uint64_t stream_out = policy_evict_first();  // q, k, v are not read again here
   uint32_t it = 0, ob = 0;
   for (int t = cl; t < total; t += ncl, ++it) {
     const PTile tl = decode(p, t, rank);
@@ -286,7 +290,7 @@ __device__ void p_epilogue(const ProdParams& p, const PShared& s, int total, uin
         fence_proxy_async_smem();
         __syncwarp();
         if (lane == 0) {
-          tma_store_3d(&p.tm_out[kind], buf, d0, row0, tl.b * p.heads + h);
+          tma_store_3d_hint(&p.tm_out[kind], buf, d0, row0, tl.b * p.heads + h, stream_out);
           bulk_commit_group();
         }
         ob ^= 1u;
