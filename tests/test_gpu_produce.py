@@ -63,6 +63,8 @@ CASES = [
     ("d128_bn128", 1, 3, 128, 2, 1, 64, 8, 128),              # H*D=384: BN=128
     ("d64_bn256_four_heads", 2, 4, 64, 3, 1, 48, 8, 320),     # four heads per tile, N=192
     ("short_single_tile", 1, 2, 128, 2, 1, 16, 4, 64),        # N=48 < 128, one k-step
+    ("odd_tile_count_batch2", 2, 2, 128, 5, 1, 48, 8, 192),   # N=288: 3 token tiles, the
+                                                              # pair's second CTA idles on the last
 ]
 
 
@@ -157,3 +159,25 @@ def test_produce_argument_errors():
     with pytest.raises(fw.WsattnError) as e:
         fw.wsattn_produce(_plan(wl1), x1.cuda(), w1.cuda(), c1.cuda(), s1.cuda())
     assert e.value.code == 3
+
+
+@pytest.mark.parametrize("flags", [0, 1])
+def test_produce_window_bound_statistics(flags):
+    # with window row bounds (and a causal variant) the folded statistics
+    # still equal wsattn_prepare's on the same tensors
+    import frame_aligned_window_gb300 as fw
+    wl = Workload("win", 2, 2, 128, 6, 1, 48, 1, 91 + flags, grid_w=8)
+    x, w, c, s = producer_inputs(wl, 128)
+    plans = []
+    for _ in range(2):
+        pl = fw.wsattn_plan(wl.frames, wl.tokens_per_frame, wl.window, wl.ref_frames, wl.heads,
+                            wl.head_dim, 0, 0, flags)
+        fw.wsattn_plan_set_bound(pl, fw.BOUND_WINDOW)
+        plans.append(pl)
+    q, k, v = fw.wsattn_produce(plans[0], x.cuda(), w.cuda(), c.cuda(), s.cuda(), EPS)
+    fw.wsattn_prepare(plans[1], q, k)
+    st, st2 = (fw.wsattn_get_stats(pl, wl.batch) for pl in plans)
+    assert fw.wsattn_device_status(plans[0]) == 0
+    np.testing.assert_array_equal(st["elig"], st2["elig"])
+    for key in ("mu", "kmax", "b", "m", "bmax"):
+        np.testing.assert_allclose(st[key], st2[key], rtol=1e-5, atol=1e-6)
