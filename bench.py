@@ -170,6 +170,26 @@ def _barrier(world):
         dist.barrier()
 
 
+# ex2.approx issue rate of one SM, per clock (a probe of this build measured
+# 62 G/s per SM at about 1.94 GHz: 32 per clock).
+EX2_PER_CLK_PER_SM = 32
+
+
+def _sfu_line(wl, active_pairs: int, ms: float, clocks):
+    """The forward's exponentials per second against the SFU rate at the
+    sampled median SM clock (max clock if none was sampled)."""
+    import torch
+    n = float(active_pairs) * wl.batch * wl.heads
+    sms = torch.cuda.get_device_properties(torch.cuda.current_device()).multi_processor_count
+    summ = clocks.summary() if clocks else {}
+    mhz = summ.get("sm_mhz") or summ.get("sm_max_mhz") or 2070.0
+    peak = EX2_PER_CLK_PER_SM * sms * mhz * 1e6
+    got = n / (ms * 1e-3)
+    return {"ex2_per_call": n, "achieved_g_per_s": got / 1e9, "peak_g_per_s": peak / 1e9,
+            "frac": got / peak, "peak_source": "probe-measured 32 ex2 per clock per SM x SMs "
+                                               "x median SM clock"}
+
+
 def step_flops(wl, active_pairs: int) -> float:
     return 4.0 * wl.head_dim * active_pairs * wl.batch * wl.heads
 
@@ -443,7 +463,10 @@ def run_gpu(args, wl, world, rank, local):
                      "traffic_unit": "bytes per launch (ncu dram read + write)",
                      "algorithmic_bytes": 3 * elem * 2 + elem * 4,
                      "peak_source": f"{peaks['source']} (bf16 burst)",
-                     "ms_per_launch": fwd_avg},
+                     "ms_per_launch": fwd_avg,
+                     "ms_per_launch_median": statistics.median(fwd_ms),
+                     # the secondary limit: one ex2 per active (query, key) pair
+                     "sfu": _sfu_line(wl, plan.active_pairs, fwd_avg, clocks)},
         "prepare": {"bound": "hbm", "ms_per_call": prep_avg, "launches": 3,
                     "algorithmic_bytes": prep_bytes,
                     "achieved": prep_bytes / (prep_avg * 1e-3) / 1e9,

@@ -771,12 +771,14 @@ __global__ void timeout_selftest_kernel(long long limit_cycles, int* status) {
 
 template <int D, int MAXC>
 cudaError_t launch_one(const FwdParams& p, int grid, size_t smem, cudaStream_t stream) {
-  static bool attr_set = false;
-  if (!attr_set) {
+  static bool attr_set[kMaxDevices] = {};
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  if (!attr_set[dev]) {
     const cudaError_t e = cudaFuncSetAttribute(
         wsattn_fwd_kernel<D, MAXC>, cudaFuncAttributeMaxDynamicSharedMemorySize, 232448);
     if (e != cudaSuccess) return e;
-    attr_set = true;
+    attr_set[dev] = true;
   }
   wsattn_fwd_kernel<D, MAXC><<<grid, kThreads, smem, stream>>>(p);
   return cudaGetLastError();

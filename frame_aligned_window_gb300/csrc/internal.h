@@ -181,6 +181,14 @@ cudaError_t launch_produce(const ProdParams& p, const uint16_t* x, float eps, in
 // Self test of the bounded wait (see wsattn_selftest_timeout).
 cudaError_t launch_timeout_selftest(long long limit_cycles, int* status, cudaStream_t s);
 
+// Kernel launch attributes are set once per device (a process may drive
+// several; cudaFuncSetAttribute acts on the current one).
+constexpr int kMaxDevices = 64;
+inline int current_device() {
+  int d = 0;
+  return cudaGetDevice(&d) == cudaSuccess && d >= 0 && d < kMaxDevices ? d : -1;
+}
+
 // Device status bits.
 constexpr int kStatusTimeoutProducer = 1;
 constexpr int kStatusTimeoutMma = 2;

@@ -424,8 +424,10 @@ __global__ void __launch_bounds__(32 * kRedRows) reduce_key_sums(const float* __
 // grid: clusters beyond that would wait for a second wave).
 template <int D, int BN>
 cudaError_t launch_gemm(const ProdParams& p, int max_ctas, cudaStream_t stream) {
-  static bool attr_set = false;
-  static int max_clusters = 0;
+  static int max_clusters_of[kMaxDevices] = {};  // 0: not configured yet
+  const int dev = current_device();
+  if (dev < 0) return cudaErrorInvalidDevice;
+  int& max_clusters = max_clusters_of[dev];
   const size_t smem = produce_smem_bytes(BN);
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
@@ -438,16 +440,17 @@ cudaError_t launch_gemm(const ProdParams& p, int max_ctas, cudaStream_t stream) 
   cfg.stream = stream;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  if (!attr_set) {
+  if (max_clusters == 0) {
     cudaError_t e = cudaFuncSetAttribute(produce_kernel<D, BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
                                          static_cast<int>(smem));
     if (e != cudaSuccess) return e;
     cfg.gridDim = dim3(2);
-    e = cudaOccupancyMaxActiveClusters(&max_clusters, produce_kernel<D, BN>, &cfg);
+    int n = 0;
+    e = cudaOccupancyMaxActiveClusters(&n, produce_kernel<D, BN>, &cfg);
     if (e != cudaSuccess) return e;
-    if (max_clusters < 1) return cudaErrorInvalidConfiguration;
-    attr_set = true;
+    if (n < 1) return cudaErrorInvalidConfiguration;
+    max_clusters = n;
   }
   const int units = p.batch * p.mpairs * p.ntiles;
   int clusters = max_ctas / 2 < max_clusters ? max_ctas / 2 : max_clusters;
