@@ -70,6 +70,16 @@ __device__ __forceinline__ float block_max(float v, float* scratch) {
   return m;
 }
 
+// Max of v[0, n) (values >= 0) over the calling warp (every lane gets it):
+// lane l takes v[l], v[l + 32], ...; max is exact in any order.
+__device__ __forceinline__ float warp_max_of(const float* __restrict__ v, int n) {
+  float m = 0.f;
+  for (int i = threadIdx.x & 31; i < n; i += 32) m = fmaxf(m, v[i]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPrepThreads)
     prep_pass_a(const uint16_t* __restrict__ k, int64_t n, int rpc, int nchunk,
@@ -122,9 +132,19 @@ __global__ void __launch_bounds__(kPrepThreads)
   const int bh = blockIdx.y, c = blockIdx.x;
   const int lr = threadIdx.x % kLanes, rs = threadIdx.x / kLanes;
   if (threadIdx.x < D) {
-    float s = 0.f;
-    for (int cc = 0; cc < nsum; ++cc)
-      s += part_sum[(static_cast<size_t>(bh) * nsum + cc) * D + threadIdx.x];
+    // four interleaved partial sums keep four loads in flight; they combine
+    // in a fixed order, so the mean stays reproducible
+    const float* ps = part_sum + static_cast<size_t>(bh) * nsum * D + threadIdx.x;
+    float a0 = 0.f, a1 = 0.f, a2 = 0.f, a3 = 0.f;
+    int cc = 0;
+    for (; cc + 3 < nsum; cc += 4) {
+      a0 += ps[static_cast<size_t>(cc) * D];
+      a1 += ps[static_cast<size_t>(cc + 1) * D];
+      a2 += ps[static_cast<size_t>(cc + 2) * D];
+      a3 += ps[static_cast<size_t>(cc + 3) * D];
+    }
+    for (; cc < nsum; ++cc) a0 += ps[static_cast<size_t>(cc) * D];
+    const float s = (a0 + a1) + (a2 + a3);
     const float m = s / static_cast<float>(n);
     mu_s[threadIdx.x] = m;
     if (c == 0) mu_out[static_cast<size_t>(bh) * D + threadIdx.x] = m;
@@ -196,11 +216,9 @@ __global__ void __launch_bounds__(kPrepThreads)
                 float* __restrict__ bmax, uint8_t* __restrict__ elig) {
   __shared__ float k_s;
   const int bh = blockIdx.y, c = blockIdx.x;
-  if (threadIdx.x == 0) {
-    float kh = 0.f;
-    for (int cc = 0; cc < nchunk; ++cc)
-      kh = fmaxf(kh, part_kmax[static_cast<size_t>(bh) * nchunk + cc]);
-    k_s = kh;
+  if (threadIdx.x < 32) {
+    const float kh = warp_max_of(part_kmax + static_cast<size_t>(bh) * nchunk, nchunk);
+    if (threadIdx.x == 0) k_s = kh;
   }
   __syncthreads();
   const float kh = k_s;
@@ -212,10 +230,9 @@ __global__ void __launch_bounds__(kPrepThreads)
     b_rows[base + r] = b;
     m_rows[base + r] = b + m_rows[base + r];          // m_rows holds c_i here
   }
-  if (c == 0 && threadIdx.x == 0) {
-    float qm = 0.f;
-    for (int cc = 0; cc < nchunk; ++cc)
-      qm = fmaxf(qm, part_qmax[static_cast<size_t>(bh) * nchunk + cc]);
+  if (c == 0 && threadIdx.x < 32) {
+    const float qm = warp_max_of(part_qmax + static_cast<size_t>(bh) * nchunk, nchunk);
+    if (threadIdx.x != 0) return;
     const float bm = (scale * qm) * kh;
     const float underflow_limit = 126.0f * 0.693147180559945309f;
     kmax[bh] = kh;
@@ -244,7 +261,14 @@ __global__ void __launch_bounds__(kPrepThreads)
       if (frames_interact(f, g, F, w, R, flags)) kh = fmaxf(kh, pk[g]);
     return kh;
   };
-  if (threadIdx.x == 0) k_s = window_max(a);
+  if (threadIdx.x < 32) {  // the warp's lanes take the key frames g = lane, lane + 32, ...
+    float kh = 0.f;
+    for (int g = threadIdx.x; g < nchunk; g += 32)
+      if (frames_interact(a, g, F, w, R, flags)) kh = fmaxf(kh, pk[g]);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) kh = fmaxf(kh, __shfl_xor_sync(0xffffffffu, kh, o));
+    if (threadIdx.x == 0) k_s = kh;
+  }
   __syncthreads();
   const float kh = k_s;
   const int64_t r0 = static_cast<int64_t>(a) * rpc;
@@ -255,12 +279,18 @@ __global__ void __launch_bounds__(kPrepThreads)
     b_rows[base + r] = b;
     m_rows[base + r] = b + m_rows[base + r];          // m_rows holds c_i here
   }
-  if (a == 0 && threadIdx.x == 0) {
+  if (a == 0 && threadIdx.x < 32) {  // lanes take the query frames; max is order-free
     float kg = 0.f, bm = 0.f;
-    for (int f = 0; f < nchunk; ++f) {
+    for (int f = threadIdx.x; f < nchunk; f += 32) {
       kg = fmaxf(kg, pk[f]);
       bm = fmaxf(bm, (scale * part_qmax[static_cast<size_t>(bh) * nchunk + f]) * window_max(f));
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      kg = fmaxf(kg, __shfl_xor_sync(0xffffffffu, kg, o));
+      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
+    }
+    if (threadIdx.x != 0) return;
     const float underflow_limit = 126.0f * 0.693147180559945309f;
     kmax[bh] = kg;
     bmax[bh] = bm;
