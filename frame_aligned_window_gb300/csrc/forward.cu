@@ -732,6 +732,7 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   const uint32_t tbase = *tslot;
+  griddep_wait();  // the row maxima and eligibility come from the kernel before
 
   if (warp == 0) {
     if (lane == 0) producer<D>(p, s);
@@ -780,8 +781,10 @@ cudaError_t launch_one(const FwdParams& p, int grid, size_t smem, cudaStream_t s
     if (e != cudaSuccess) return e;
     attr_set[dev] = true;
   }
-  wsattn_fwd_kernel<D, MAXC><<<grid, kThreads, smem, stream>>>(p);
-  return cudaGetLastError();
+  // dependent launch: the prologue (barriers, TMEM, tensor maps) overlaps
+  // the end of the statistics pass before it
+  return launch_dependent(wsattn_fwd_kernel<D, MAXC>, dim3(grid), dim3(kThreads), smem, stream,
+                          p);
 }
 
 template <int D, int M>

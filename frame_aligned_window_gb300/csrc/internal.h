@@ -181,6 +181,26 @@ cudaError_t launch_produce(const ProdParams& p, const uint16_t* x, float eps, in
 // Self test of the bounded wait (see wsattn_selftest_timeout).
 cudaError_t launch_timeout_selftest(long long limit_cycles, int* status, cudaStream_t s);
 
+// Launches `kernel` with programmatic stream serialization: it may begin
+// while the previous kernel in the stream is finishing, and each of its
+// threads calls ptx::griddep_wait() before reading that kernel's results or
+// writing anything an earlier kernel may still read.
+template <typename... KArgs, typename... Args>
+cudaError_t launch_dependent(void (*kernel)(KArgs...), dim3 grid, dim3 block, size_t smem,
+                             cudaStream_t stream, Args... args) {
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.gridDim = grid;
+  cfg.blockDim = block;
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = stream;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, static_cast<KArgs>(args)...);
+}
+
 // Kernel launch attributes are set once per device (a process may drive
 // several; cudaFuncSetAttribute acts on the current one).
 constexpr int kMaxDevices = 64;

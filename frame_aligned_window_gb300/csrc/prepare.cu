@@ -31,6 +31,7 @@
 #include <cuda_bf16.h>
 
 #include "internal.h"
+#include "ptx.cuh"
 
 namespace wsattn {
 namespace {
@@ -129,6 +130,7 @@ __global__ void __launch_bounds__(kPrepThreads)
   constexpr int kRows = kPrepThreads / kLanes;
   __shared__ float mu_s[D];
   __shared__ float wmax[kPrepThreads / 32];
+  ptx::griddep_wait();  // the key sums come from the previous kernel
   const int bh = blockIdx.y, c = blockIdx.x;
   const int lr = threadIdx.x % kLanes, rs = threadIdx.x / kLanes;
   if (threadIdx.x < D) {
@@ -215,6 +217,7 @@ __global__ void __launch_bounds__(kPrepThreads)
                 const float* __restrict__ part_qmax, float* __restrict__ kmax,
                 float* __restrict__ bmax, uint8_t* __restrict__ elig) {
   __shared__ float k_s;
+  ptx::griddep_wait();  // the chunk maxima and row values come from pass B
   const int bh = blockIdx.y, c = blockIdx.x;
   if (threadIdx.x < 32) {
     const float kh = warp_max_of(part_kmax + static_cast<size_t>(bh) * nchunk, nchunk);
@@ -253,6 +256,7 @@ __global__ void __launch_bounds__(kPrepThreads)
                        float* __restrict__ kmax, float* __restrict__ bmax,
                        uint8_t* __restrict__ elig) {
   __shared__ float k_s;
+  ptx::griddep_wait();  // the chunk maxima and row values come from pass B
   const int bh = blockIdx.y, a = blockIdx.x;
   const float* pk = part_kmax + static_cast<size_t>(bh) * nchunk;
   auto window_max = [&](int f) {
@@ -323,30 +327,36 @@ cudaError_t launch_prepare(const void* q, const void* k, int BH, int64_t N, int 
   // key column sums: pass A's per-chunk sums, or one row per head given
   const float* sums = key_sums ? key_sums : b.part_sum;
   const int nsum = key_sums ? 1 : b.nchunk;
+  // pass A is an ordinary launch; B and C may start while their predecessor
+  // finishes and wait for it on the device
+  cudaError_t e = cudaSuccess;
   if (D == 128) {
     if (!key_sums)
       prep_pass_a<128><<<grid, kPrepThreads, 0, stream>>>(k16, N, b.rows_per_chunk, b.nchunk,
                                                           b.part_sum);
-    prep_pass_b<128><<<grid, kPrepThreads, 0, stream>>>(
-        q16, k16, N, b.rows_per_chunk, b.nchunk, scale, sums, nsum, b.mu, b.b_rows, b.m_rows,
-        b.part_kmax, b.part_qmax);
+    e = launch_dependent(prep_pass_b<128>, grid, dim3(kPrepThreads), 0, stream, q16, k16, N,
+                         b.rows_per_chunk, b.nchunk, scale, sums, nsum, b.mu, b.b_rows, b.m_rows,
+                         b.part_kmax, b.part_qmax);
   } else {
     if (!key_sums)
       prep_pass_a<64><<<grid, kPrepThreads, 0, stream>>>(k16, N, b.rows_per_chunk, b.nchunk,
                                                          b.part_sum);
-    prep_pass_b<64><<<grid, kPrepThreads, 0, stream>>>(
-        q16, k16, N, b.rows_per_chunk, b.nchunk, scale, sums, nsum, b.mu, b.b_rows, b.m_rows,
-        b.part_kmax, b.part_qmax);
+    e = launch_dependent(prep_pass_b<64>, grid, dim3(kPrepThreads), 0, stream, q16, k16, N,
+                         b.rows_per_chunk, b.nchunk, scale, sums, nsum, b.mu, b.b_rows, b.m_rows,
+                         b.part_kmax, b.part_qmax);
   }
-  if (win)
-    prep_pass_c_window<<<grid, kPrepThreads, 0, stream>>>(
-        N, b.rows_per_chunk, b.nchunk, win->F, win->R, win->w, win->flags, scale, tau, b.b_rows,
-        b.m_rows,
-        b.part_kmax, b.part_qmax, b.kmax, b.bmax, b.elig);
-  else
-    prep_pass_c<<<grid, kPrepThreads, 0, stream>>>(N, b.rows_per_chunk, b.nchunk, scale, tau,
-                                                   b.b_rows, b.m_rows, b.part_kmax, b.part_qmax,
-                                                   b.kmax, b.bmax, b.elig);
+  if (e != cudaSuccess) return e;
+  if (win) {
+    e = launch_dependent(prep_pass_c_window, grid, dim3(kPrepThreads), 0, stream, N,
+                         b.rows_per_chunk, b.nchunk, win->F, win->R, win->w, win->flags, scale,
+                         tau, b.b_rows, b.m_rows, b.part_kmax, b.part_qmax, b.kmax, b.bmax,
+                         b.elig);
+  } else {
+    e = launch_dependent(prep_pass_c, grid, dim3(kPrepThreads), 0, stream, N, b.rows_per_chunk,
+                         b.nchunk, scale, tau, b.b_rows, b.m_rows, b.part_kmax, b.part_qmax,
+                         b.kmax, b.bmax, b.elig);
+  }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

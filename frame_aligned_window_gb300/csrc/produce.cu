@@ -216,6 +216,7 @@ __device__ void p_epilogue(const ProdParams& p, const PShared& s, int total, uin
   const uint32_t tlane = tbase + (static_cast<uint32_t>(32 * wq) << 16);
   const int hd = p.heads * D;
   const uint64_t stream_out = policy_evict_first();  // q, k, v are not read again here
+  griddep_wait();  // 1/rms comes from the pre-pass, which may still be running
   uint32_t it = 0, ob = 0;
   for (int t = cl; t < total; t += ncl, ++it) {
     const PTile tl = decode(p, t, rank);
@@ -397,6 +398,7 @@ __global__ void __launch_bounds__(32 * kRedRows) reduce_key_sums(const float* __
                                                                  int nparts, int D,
                                                                  float* __restrict__ out) {
   __shared__ float red[kRedRows][32];
+  griddep_wait();  // the group sums come from the GEMM's epilogue
   const int bh = blockIdx.y, c = 32 * blockIdx.x + threadIdx.x, g = threadIdx.y;
   const float* src = parts + static_cast<size_t>(bh) * nparts * D + c;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
@@ -430,16 +432,20 @@ cudaError_t launch_gemm(const ProdParams& p, int max_ctas, cudaStream_t stream) 
   int& max_clusters = max_clusters_of[dev];
   const size_t smem = produce_smem_bytes(BN);
   cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[1];
+  cudaLaunchAttribute attr[2];
   attr[0].id = cudaLaunchAttributeClusterDimension;
   attr[0].val.clusterDim.x = 2;
   attr[0].val.clusterDim.y = 1;
   attr[0].val.clusterDim.z = 1;
+  // dependent launch: the GEMM's main loop (x and W only) overlaps the RMS
+  // pre-pass; the epilogue waits for its 1/rms values
+  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[1].val.programmaticStreamSerializationAllowed = 1;
   cfg.blockDim = dim3(kPThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = stream;
   cfg.attrs = attr;
-  cfg.numAttrs = 1;
+  cfg.numAttrs = 1;  // the occupancy query takes the cluster shape alone
   if (max_clusters == 0) {
     cudaError_t e = cudaFuncSetAttribute(produce_kernel<D, BN>,
                                          cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -457,6 +463,7 @@ cudaError_t launch_gemm(const ProdParams& p, int max_ctas, cudaStream_t stream) 
   if (clusters > units) clusters = units;
   if (clusters < 1) clusters = 1;
   cfg.gridDim = dim3(2 * clusters);
+  cfg.numAttrs = 2;
   return cudaLaunchKernelEx(&cfg, produce_kernel<D, BN>, p);
 }
 
@@ -487,9 +494,8 @@ cudaError_t launch_produce(const ProdParams& p, const uint16_t* x, float eps, in
     e = bn == 256 ? launch_gemm<64, 256>(p, grid, stream) : launch_gemm<64, 128>(p, grid, stream);
   if (e != cudaSuccess) return e;
   const int BH = p.batch * p.heads;
-  reduce_key_sums<<<dim3(D / 32, BH), dim3(32, kRedRows), 0, stream>>>(p.part_sum, p.nparts, D,
-                                                                      key_sums);
-  return cudaGetLastError();
+  return launch_dependent(reduce_key_sums, dim3(D / 32, BH), dim3(32, kRedRows), 0, stream,
+                          static_cast<const float*>(p.part_sum), p.nparts, D, key_sums);
 }
 
 }  // namespace wsattn
