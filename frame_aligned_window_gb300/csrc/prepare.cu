@@ -88,6 +88,7 @@ __global__ void __launch_bounds__(kPrepThreads)
   constexpr int kLanes = D / 8;                 // threads sharing one row
   constexpr int kRows = kPrepThreads / kLanes;  // rows in flight per CTA
   __shared__ float red[kRows][D];
+  ptx::griddep_wait();  // whatever ran before may still read part_sum or write k
   const int bh = blockIdx.y, c = blockIdx.x;
   const int lr = threadIdx.x % kLanes, rs = threadIdx.x / kLanes;
   const int64_t r0 = static_cast<int64_t>(c) * rpc;
@@ -327,20 +328,22 @@ cudaError_t launch_prepare(const void* q, const void* k, int BH, int64_t N, int 
   // key column sums: pass A's per-chunk sums, or one row per head given
   const float* sums = key_sums ? key_sums : b.part_sum;
   const int nsum = key_sums ? 1 : b.nchunk;
-  // pass A is an ordinary launch; B and C may start while their predecessor
-  // finishes and wait for it on the device
+  // every pass may start while its predecessor finishes and waits for it
+  // on the device
   cudaError_t e = cudaSuccess;
   if (D == 128) {
     if (!key_sums)
-      prep_pass_a<128><<<grid, kPrepThreads, 0, stream>>>(k16, N, b.rows_per_chunk, b.nchunk,
-                                                          b.part_sum);
+      e = launch_dependent(prep_pass_a<128>, grid, dim3(kPrepThreads), 0, stream, k16, N,
+                           b.rows_per_chunk, b.nchunk, b.part_sum);
+    if (e != cudaSuccess) return e;
     e = launch_dependent(prep_pass_b<128>, grid, dim3(kPrepThreads), 0, stream, q16, k16, N,
                          b.rows_per_chunk, b.nchunk, scale, sums, nsum, b.mu, b.b_rows, b.m_rows,
                          b.part_kmax, b.part_qmax);
   } else {
     if (!key_sums)
-      prep_pass_a<64><<<grid, kPrepThreads, 0, stream>>>(k16, N, b.rows_per_chunk, b.nchunk,
-                                                         b.part_sum);
+      e = launch_dependent(prep_pass_a<64>, grid, dim3(kPrepThreads), 0, stream, k16, N,
+                           b.rows_per_chunk, b.nchunk, b.part_sum);
+    if (e != cudaSuccess) return e;
     e = launch_dependent(prep_pass_b<64>, grid, dim3(kPrepThreads), 0, stream, q16, k16, N,
                          b.rows_per_chunk, b.nchunk, scale, sums, nsum, b.mu, b.b_rows, b.m_rows,
                          b.part_kmax, b.part_qmax);
