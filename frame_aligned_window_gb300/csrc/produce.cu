@@ -367,6 +367,8 @@ __global__ void __launch_bounds__(kPThreads, 1) produce_kernel(const __grid_cons
 // the lanes combine in a fixed butterfly, so the result is reproducible.
 __global__ void __launch_bounds__(256) rms_kernel(const uint16_t* __restrict__ x, int64_t rows,
                                                   int C, float eps, float* __restrict__ inv) {
+  // the GEMM that follows reads only x and W until its epilogue: let it start
+  griddep_launch_dependents();
   const int64_t row = static_cast<int64_t>(blockIdx.x) * 8 + threadIdx.x / 32;
   const int lane = threadIdx.x & 31;
   if (row >= rows) return;
