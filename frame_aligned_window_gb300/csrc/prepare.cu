@@ -160,14 +160,22 @@ __global__ void __launch_bounds__(kPrepThreads)
   const int64_t r1 = min(n, r0 + rpc);
   const size_t base = static_cast<size_t>(bh) * n;
   float km = 0.f, qm = 0.f;
-  for (int64_t rb = r0; rb < r1; rb += kRows * kUnroll) {  // uniform trip count per warp
+  // Row groups in reverse order: pass A just streamed this chunk's keys in
+  // forward order, so the most recently read ones (the likeliest still in
+  // L2) come first.  q is read once here: evict-first, no L1 allocation.
+  const uint64_t q_policy = ptx::policy_evict_first();
+  constexpr int64_t kGroup = kRows * kUnroll;
+  const int64_t n_groups = (r1 - r0 + kGroup - 1) / kGroup;
+  for (int64_t g = n_groups - 1; g >= 0; --g) {  // uniform trip count per warp
+    const int64_t rb = r0 + g * kGroup;
     uint4 kv[kUnroll], qv[kUnroll];
 #pragma unroll
     for (int u = 0; u < kUnroll; ++u) {
       const int64_t r = rb + u * kRows + rs;
       if (r < r1) {
         kv[u] = __ldg(reinterpret_cast<const uint4*>(k + (base + r) * D) + lr);
-        qv[u] = __ldg(reinterpret_cast<const uint4*>(q + (base + r) * D) + lr);
+        qv[u] = ptx::ld_stream_v4(reinterpret_cast<const uint4*>(q + (base + r) * D) + lr,
+                                  q_policy);
       } else {
         kv[u] = make_uint4(0u, 0u, 0u, 0u);
         qv[u] = kv[u];

@@ -82,6 +82,14 @@ __device__ __forceinline__ uint64_t policy_evict_first() {
   asm volatile("createpolicy.fractional.L2::evict_first.b64 %0, 1.0;" : "=l"(p));
   return p;
 }
+// 16-byte global load that skips L1 and marks its L2 lines with `policy`.
+__device__ __forceinline__ uint4 ld_stream_v4(const uint4* p, uint64_t policy) {
+  uint4 v;
+  asm volatile("ld.global.L1::no_allocate.L2::cache_hint.v4.u32 {%0, %1, %2, %3}, [%4], %5;"
+               : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "l"(p), "l"(policy));
+  return v;
+}
 // tma_load_2d_mc with an L2 eviction policy for the loaded lines.
 __device__ __forceinline__ void tma_load_2d_mc_hint(uint32_t dst, const CUtensorMap* map,
                                                     uint32_t bar, int32_t x, int32_t y,
