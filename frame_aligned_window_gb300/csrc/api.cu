@@ -7,6 +7,7 @@
 #include <cstring>
 #include <mutex>
 #include <new>
+#include <vector>
 
 #include "internal.h"
 
@@ -32,6 +33,10 @@ struct wsattn_plan_s {
   int force_path = -1;
   float tau = wsattn::kDefaultTau;
   int bound_mode = WSATTN_BOUND_GLOBAL;
+  // forward work schedule for (sched_bh, sched_grid)
+  int32_t* d_sched = nullptr;
+  size_t sched_cap = 0;  // int32 entries allocated
+  int sched_bh = 0, sched_grid = 0;
   // producer workspace (inverse RMS per token, key sums), sized for prod_batch
   int prod_batch = 0;
   void* prod_ws = nullptr;
@@ -226,9 +231,38 @@ int ensure_prod_workspace(wsattn_plan_s* p, int batch, cudaStream_t stream) {
   return WSATTN_OK;
 }
 
+// The forward's per-CTA work lists for BH heads on `grid` CTAs (host-built
+// once per batch size; the upload synchronises the stream).
+int ensure_schedule(wsattn_plan_s* p, int BH, int grid, cudaStream_t stream) {
+  if (p->d_sched && p->sched_bh == BH && p->sched_grid == grid) return WSATTN_OK;
+  std::vector<int32_t> h;
+  try {
+    h = wsattn::build_schedule(p->hp, BH, grid);
+  } catch (const std::bad_alloc&) {
+    return WSATTN_ERR_NO_MEMORY;
+  }
+  if (cudaStreamSynchronize(stream) != cudaSuccess) return WSATTN_ERR_CUDA;
+  if (h.size() > p->sched_cap) {
+    if (p->d_sched) cudaFree(p->d_sched);
+    p->d_sched = nullptr;
+    p->sched_cap = 0;
+    if (cudaMalloc(&p->d_sched, h.size() * sizeof(int32_t)) != cudaSuccess) return WSATTN_ERR_CUDA;
+    p->sched_cap = h.size();
+  }
+  if (cudaMemcpy(p->d_sched, h.data(), h.size() * sizeof(int32_t), cudaMemcpyHostToDevice) !=
+      cudaSuccess)
+    return WSATTN_ERR_CUDA;
+  p->sched_bh = BH;
+  p->sched_grid = grid;
+  return WSATTN_OK;
+}
+
 void free_device(wsattn_plan_s* p) {
   if (p->prod_ws) cudaFree(p->prod_ws);
   p->prod_ws = nullptr;
+  if (p->d_sched) cudaFree(p->d_sched);
+  p->d_sched = nullptr;
+  p->sched_cap = 0;
   if (p->d_tiles) cudaFree(p->d_tiles);
   if (p->d_cls) cudaFree(p->d_cls);
   if (p->d_status) cudaFree(p->d_status);
@@ -412,6 +446,9 @@ int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, 
   if (prm.stages_k < 2 || smem > plan->smem_optin) return WSATTN_ERR_UNSUPPORTED;
   const int64_t items = static_cast<int64_t>(prm.n_tiles) * BH;
   const int grid = static_cast<int>(items < plan->num_sms ? items : plan->num_sms);
+  rc = ensure_schedule(plan, BH, grid, static_cast<cudaStream_t>(stream));
+  if (rc != WSATTN_OK) return rc;
+  prm.sched = plan->d_sched;
   if (wsattn::launch_forward(prm, hp.D, grid, smem, static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return WSATTN_ERR_CUDA;

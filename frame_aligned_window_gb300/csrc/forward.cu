@@ -192,6 +192,19 @@ __device__ __forceinline__ Item map_item(const FwdParams& p, int it) {
   return Item{beg + o % n, o / n};
 }
 
+// This CTA's work items in order, from the host-built schedule (every role
+// of the CTA walks the same list).
+struct WorkList {
+  const int32_t* items;
+  int n;
+  __device__ __forceinline__ explicit WorkList(const FwdParams& p) {
+    const int b = __ldg(p.sched + blockIdx.x), e = __ldg(p.sched + blockIdx.x + 1);
+    items = p.sched + gridDim.x + 1 + b;
+    n = e - b;
+  }
+  __device__ __forceinline__ int operator[](int k) const { return __ldg(items + k); }
+};
+
 // Position in a ring of `n` stages: slot and the parity of its current use.
 // Advanced by increments only (no division in the per-step loops).
 struct Ring {
@@ -240,11 +253,12 @@ __device__ void producer(const FwdParams& p, const Shared& s) {
   const uint32_t ns = static_cast<uint32_t>(G * bk);     // rows of a step
   const uint32_t box_pitch = ns * 128u;                  // a 64-column box of a stage
   const uint32_t stage_bytes = box_pitch * kBoxes;
-  const int n_items = p.n_tiles * p.bh;
   const uint32_t nk = static_cast<uint32_t>(p.stages_k), nv = static_cast<uint32_t>(p.stages_v);
   Ring kr, vr;
   uint32_t qc = 0;
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+  const WorkList wl(p);
+  for (int w = 0; w < wl.n; ++w) {
+    const int it = wl[w];
     const Item im = map_item(p, it);
     const WorkTile t = p.tiles[im.tile];
     const int y0 = im.bh * p.n;
@@ -308,13 +322,14 @@ __device__ void qk_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
   // K is K-major (SBO 1 KB)
   const uint64_t kdesc0 = sdesc_sw128(s.k, 16, 1024);
   const uint64_t box16 = box_pitch >> 4, stage16 = stage_bytes >> 4;
-  const int n_items = p.n_tiles * p.bh;
   const uint32_t nk = static_cast<uint32_t>(p.stages_k);
   Ring kr;
   uint32_t su = 0;  // parity of the current use of S
   uint32_t tiles_done = 0;
   Steps qs;
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+  const WorkList wl(p);
+  for (int w = 0; w < wl.n; ++w) {
+    const int it = wl[w];
     const Item im = map_item(p, it);
     const WorkTile t = p.tiles[im.tile];
     qs.init(t);
@@ -358,11 +373,12 @@ __device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
   // V is MN-major (LBO = the 64-column box pitch)
   const uint64_t vdesc0 = sdesc_sw128(s.v, box_pitch, 1024);
   const uint64_t stage16 = stage_bytes >> 4;
-  const int n_items = p.n_tiles * p.bh;
   const uint32_t nv = static_cast<uint32_t>(p.stages_v);
   Ring vr, pr;
   Steps ps;
-  for (int it = blockIdx.x; it < n_items; it += gridDim.x) {
+  const WorkList wl(p);
+  for (int w = 0; w < wl.n; ++w) {
+    const int it = wl[w];
     const Item im = map_item(p, it);
     const WorkTile t = p.tiles[im.tile];
     const int nstep = t.nstep;
@@ -493,8 +509,9 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
   uint32_t su = 0;  // parity of the current use of S
   Ring pr;          // P buffer
 
-  int it = blockIdx.x;
-  if (it >= n_items) return;
+  const WorkList wl(p);
+  if (wl.n == 0) return;
+  int w = 0, it = wl[0];
   if (!load_q<D>(s, lane + tc_.q, wg, r, p.tiles[map_item(p, it).tile].nvalid, qc)) return;
   while (true) {
     const Item im = map_item(p, it);
@@ -610,7 +627,7 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
     }
 
     // Stage the next tile's Q so its first QK products overlap this epilogue.
-    const int nxt = it + static_cast<int>(gridDim.x);
+    const int nxt = w + 1 < wl.n ? wl[w + 1] : n_items;
     if (nxt < n_items &&
         !load_q<D>(s, lane + tc_.q, wg, r, p.tiles[map_item(p, nxt).tile].nvalid, qc))
       return;
@@ -671,6 +688,7 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
     }
     if (nxt >= n_items) break;
     it = nxt;
+    ++w;
   }
 }
 
