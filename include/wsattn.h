@@ -178,8 +178,11 @@ int wsattn_produce(wsattn_plan_t plan, int batch, const void* x, int model_dim,
  *   v    bf16 [batch, H, N, D]
  *   out  fp32 [batch, H, N, D], fully overwritten
  * Requires a prior wsattn_prepare on this plan with the same batch.
+ * The first call for a batch size builds the kernel's work schedule on the
+ * host (each CTA's list of query tiles, longest-processing-time first) and
+ * uploads it, which synchronises `stream`; make it outside stream capture.
  * Errors: BAD_ARG, NOT_PREPARED, BATCH_MISMATCH, UNSUPPORTED (block_k > 160),
- *         CUDA.
+ *         NO_MEMORY, CUDA.
  */
 int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, const void* v,
                    float* out, void* stream);
