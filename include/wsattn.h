@@ -27,7 +27,9 @@
  *   - softmax scale = 1 / sqrt(head_dim).
  *   - `stream` is a cudaStream_t (NULL = legacy default stream); all device
  *     work is enqueued on it.  No call synchronises the host except the
- *     wsattn_get_* readers and wsattn_device_status, which say so.
+ *     wsattn_get_* readers and wsattn_device_status, and the calls that grow
+ *     a plan's workspace or build its forward schedule (the first call for a
+ *     larger batch); each says so.
  *   - Every call returns a status code (WSATTN_OK = 0 or one of the errors
  *     below) and never throws or aborts.  Argument errors are reported before
  *     any work is enqueued.  Asynchronous device errors (CUDA faults, expired
