@@ -246,6 +246,20 @@ struct Steps {
 // A step's G blocks are consecutive rows of one run, so each step is one TMA
 // box per 64-column slab (G * bk rows).  The shorter last step of a run
 // loads the whole box too: the rows past it are never read by an MMA.
+// After an expired wait: the TMA loads this producer issued land in shared
+// memory whatever the consumers do, so wait (bounded) for each slot's last
+// load before the CTA may leave.
+// Bit i of `issued` marks slot i as loaded at least once, bit i of `phase`
+// the parity of its last load.
+__device__ __noinline__ void drain_loads(uint32_t full0, int n, uint32_t phase, uint32_t issued) {
+  for (int i = 0; i < n; ++i) {
+    if (!(issued >> i & 1u)) continue;
+    const long long t0 = clock64();
+    while (!mbar_try_wait(full0 + 8u * static_cast<uint32_t>(i), phase >> i & 1u))
+      if (clock64() - t0 > kWaitLimitCycles) break;
+  }
+}
+
 template <int D>
 __device__ void producer(const FwdParams& p, const Shared& s) {
   constexpr int kBoxes = D / 64;
@@ -256,13 +270,20 @@ __device__ void producer(const FwdParams& p, const Shared& s) {
   const uint32_t nk = static_cast<uint32_t>(p.stages_k), nv = static_cast<uint32_t>(p.stages_v);
   Ring kr, vr;
   uint32_t qc = 0;
+  // parity of the last load issued into each K / V slot (for drain_loads)
+  uint32_t kph = 0, vph = 0, kiss = 0, viss = 0;
+  auto drain = [&]() {
+    drain_loads(bar(s, B_KFULL0), static_cast<int>(nk), kph, kiss);
+    drain_loads(bar(s, B_VFULL0), static_cast<int>(nv), vph, viss);
+    drain_loads(bar(s, B_QFULL), 1, (qc - 1u) & 1u, qc > 0 ? 1u : 0u);
+  };
   const WorkList wl(p);
   for (int w = 0; w < wl.n; ++w) {
     const int it = wl[w];
     const Item im = map_item(p, it);
     const WorkTile t = p.tiles[im.tile];
     const int y0 = im.bh * p.n;
-    if (!wait(s, bar(s, B_QEMPTY), (qc & 1u) ^ 1u, kStatusTimeoutProducer)) return;
+    if (!wait(s, bar(s, B_QEMPTY), (qc & 1u) ^ 1u, kStatusTimeoutProducer)) return drain();
     mbar_arrive_expect_tx(bar(s, B_QFULL), kTileM * D * 2);
 #pragma unroll
     for (int c = 0; c < kBoxes; ++c)
@@ -276,23 +297,29 @@ __device__ void producer(const FwdParams& p, const Shared& s) {
       if (j < t.nstep) {
         int nb;
         const int row = y0 + ks.next(G, nb) * bk;
-        if (!wait(s, bar(s, B_KEMPTY0 + kr.slot), kr.phase ^ 1u, kStatusTimeoutProducer)) return;
+        if (!wait(s, bar(s, B_KEMPTY0 + kr.slot), kr.phase ^ 1u, kStatusTimeoutProducer))
+          return drain();
         const uint32_t fb = bar(s, B_KFULL0 + kr.slot);
         mbar_arrive_expect_tx(fb, stage_bytes);
         const uint32_t dst = s.k + kr.slot * stage_bytes;
 #pragma unroll
         for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_k, fb, c * 64, row);
+        kph = (kph & ~(1u << kr.slot)) | (kr.phase << kr.slot);
+        kiss |= 1u << kr.slot;
         kr.next(nk);
       }
       if (j >= 1) {
         int nb;
         const int row = y0 + vs.next(G, nb) * bk;
-        if (!wait(s, bar(s, B_VEMPTY0 + vr.slot), vr.phase ^ 1u, kStatusTimeoutProducer)) return;
+        if (!wait(s, bar(s, B_VEMPTY0 + vr.slot), vr.phase ^ 1u, kStatusTimeoutProducer))
+          return drain();
         const uint32_t fb = bar(s, B_VFULL0 + vr.slot);
         mbar_arrive_expect_tx(fb, stage_bytes);
         const uint32_t dst = s.v + vr.slot * stage_bytes;
 #pragma unroll
         for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_v, fb, c * 64, row);
+        vph = (vph & ~(1u << vr.slot)) | (vr.phase << vr.slot);
+        viss |= 1u << vr.slot;
         vr.next(nv);
       }
     }

@@ -112,11 +112,23 @@ __device__ void p_producer(const ProdParams& p, const PShared& s, int total, uin
   // W is re-read for every token tile: keep it in L2 ahead of the streams
   const uint64_t keep = policy_evict_last();
   uint32_t slot = 0, phase = 0;
+  uint32_t last_phase = 0, issued = 0;  // per slot: parity of its last load, loaded yet
+  // after an expired wait: the loads already issued land whatever the
+  // consumers do; wait (bounded) for each slot's last one before leaving
+  auto drain = [&]() {
+    for (int i = 0; i < kPStages; ++i) {
+      if (!(issued >> i & 1u)) continue;
+      const long long t0 = clock64();
+      while (!mbar_try_wait(pbar(s, PB_FULL0 + i), last_phase >> i & 1u))
+        if (clock64() - t0 > kPWaitLimit) break;
+    }
+  };
   for (int t = cl; t < total; t += ncl) {
     const PTile tl = decode(p, t, rank);
     for (int kt = 0; kt < ksteps; ++kt) {
       // both CTAs' MMAs have released the slot: the peer's half may land too
-      if (!pwait(s, pbar(s, PB_EMPTY0 + slot), phase ^ 1u, kStatusTimeoutProducer)) return;
+      if (!pwait(s, pbar(s, PB_EMPTY0 + slot), phase ^ 1u, kStatusTimeoutProducer))
+        return drain();
       const uint32_t dst = s.stages + slot * kStage;
       mbar_arrive_expect_tx(pbar(s, PB_FULL0 + slot), kStage);  // own x, both W halves
       tma_load_3d(dst, &p.tm_x, pbar(s, PB_FULL0 + slot), kt * kProdTileK, tl.mt * kProdTileM,
@@ -124,6 +136,8 @@ __device__ void p_producer(const ProdParams& p, const PShared& s, int total, uin
       tma_load_2d_mc_hint(dst + kPABytes + rank * kHalfB, &p.tm_w, pbar(s, PB_FULL0 + slot),
                           kt * kProdTileK, tl.nt * BN + static_cast<int>(rank) * (BN / 2), 0x3,
                           keep);
+      last_phase = (last_phase & ~(1u << slot)) | (phase << slot);
+      issued |= 1u << slot;
       if (++slot == kPStages) {
         slot = 0;
         phase ^= 1u;
