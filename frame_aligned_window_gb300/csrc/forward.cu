@@ -40,12 +40,16 @@
 // core that the softmax waits on is thus load S(j) -> QK^T(j+1) -> S full,
 // and PV runs beside it.
 //
-// Work items (tile, b*h) go class by class (tiles with equal key lists,
-// longest first) and head by head inside a class, so the CTAs running at one
-// time stream the same head's keys and values through L2.
+// Work items (tile, b*h) are ordered class by class (tiles with equal key
+// lists, longest first) and head by head inside a class, so the CTAs running
+// at one time stream the same head's keys and values through L2; the host
+// deals that list out longest-processing-time first (build_schedule) and
+// every role of a CTA walks the CTA's own list.  The kernel is a dependent
+// launch: its prologue overlaps the end of the statistics pass before it.
 //
 // Every wait is bounded: on expiry the kernel sets a bit in the status word,
-// raises a CTA-wide abort flag, and all roles leave their loops; TMEM is
+// raises a CTA-wide abort flag, and all roles leave their loops; the TMA
+// producer first waits (bounded) for the loads it has in flight, and TMEM is
 // released on the way out.
 #include <cuda_bf16.h>
 
