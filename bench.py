@@ -344,7 +344,7 @@ def run_gpu(args, wl, world, rank, local):
     # of device buffers let the copies of one step run on their own streams
     # beside the compute of the next (inputs of step i+1 in, result of step
     # i-1 out), as a streaming caller would run it.
-    e2e_steps = max(3, min(args.steps, 20))
+    e2e_steps = max(3, min(args.steps, 50))
     q2, k2, v2 = torch.empty_like(qd), torch.empty_like(kd), torch.empty_like(vd)
     out2 = torch.empty_like(out)
     slots = [(qd, kd, vd, out), (q2, k2, v2, out2)]
