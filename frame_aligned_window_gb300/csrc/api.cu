@@ -478,6 +478,21 @@ int wsattn_get_block_map(wsattn_plan_t plan, uint8_t* host, size_t n) {
   return WSATTN_OK;
 }
 
+int wsattn_get_schedule(wsattn_plan_t plan, int batch, int grid, int32_t* host, size_t n) {
+  if (!plan || !host || batch < 1 || grid < 1) return WSATTN_ERR_BAD_ARG;
+  const int64_t BH = static_cast<int64_t>(batch) * plan->hp.H;
+  const int64_t need = grid + 1 + static_cast<int64_t>(plan->hp.tiles.size()) * BH;
+  if (BH >= (int64_t(1) << 31) || need >= (int64_t(1) << 31) || n < static_cast<size_t>(need))
+    return WSATTN_ERR_BAD_ARG;
+  try {
+    const std::vector<int32_t> v = wsattn::build_schedule(plan->hp, static_cast<int>(BH), grid);
+    std::memcpy(host, v.data(), v.size() * sizeof(int32_t));
+  } catch (const std::bad_alloc&) {
+    return WSATTN_ERR_NO_MEMORY;
+  }
+  return WSATTN_OK;
+}
+
 int wsattn_get_csr(wsattn_plan_t plan, int32_t* row_ptr, int32_t* col, size_t n_row_ptr,
                    size_t n_col) {
   if (!plan || !row_ptr || (!col && !plan->hp.col.empty())) return WSATTN_ERR_BAD_ARG;

@@ -231,6 +231,16 @@ int wsattn_plan_info(wsattn_plan_t plan, int64_t* info, int n);
  * into host memory of n bytes.  Errors: BAD_ARG if n is too small. */
 int wsattn_get_block_map(wsattn_plan_t plan, uint8_t* host, size_t n);
 
+/* Copies the forward's work schedule for `batch` on `grid` CTAs (host only;
+ * wsattn_forward launches min(#SMs, work items) CTAs): grid + 1 offsets,
+ * then the work items of CTA 0, CTA 1, ... in order, n = grid + 1 +
+ * tiles * batch * heads entries (tiles: wsattn_plan_info).  Work item i is
+ * tile i mod (class size) of its class and head (b * heads + h) as the
+ * kernel decodes it; items are dealt longest-processing-time first, each to
+ * the CTA with the least predicted work.
+ * Errors: BAD_ARG (batch or grid < 1, or n too small), NO_MEMORY. */
+int wsattn_get_schedule(wsattn_plan_t plan, int batch, int grid, int32_t* host, size_t n);
+
 /* Copies the CSR of active blocks: row_ptr[N/block_q + 1], col[nnz] (key
  * block indices, increasing within a row), into host arrays of the given
  * capacities.  Errors: BAD_ARG if a capacity is too small. */
