@@ -68,6 +68,7 @@ constexpr int kThreads = 32 * (kSoftmaxWarp0 + kSoftmaxWarps);
 constexpr int kMaxChunksAll = (10 + kNumWG - 1) / kNumWG;   // chunks a warpgroup takes at 160 keys
 constexpr long long kWaitLimitCycles = 1LL << 31;  // about one second
 constexpr float kLog2e = 1.4426950408889634f;
+constexpr float kLazyMax = 8.f;  // online path: rescale when the max grows by > 2^8
 constexpr uint32_t kTmemCols = 512;
 
 // mbarrier slots
@@ -75,7 +76,6 @@ enum : int {
   B_QFULL = 0,   // TMA -> softmax: Q tile staged in smem
   B_QEMPTY,      // softmax -> TMA: Q staging buffer free
   B_QTFULL,      // softmax -> MMA: Q tile in TMEM
-  B_OBAR,        // MMA -> softmax: PV(j) done (online path only)
   B_OFULL,       // MMA -> softmax: last PV of the tile done
   B_XCH,         // softmax <-> softmax: row maxima / row sums exchanged
   B_SFULL,       // MMA -> softmax: S written (one phase per key step)
@@ -413,7 +413,6 @@ __device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
     const Item im = map_item(p, it);
     const WorkTile t = p.tiles[im.tile];
     const int nstep = t.nstep;
-    const bool online = p.force_path >= 0 ? (p.force_path == 1) : (p.elig[im.bh] == 0);
     ps.init(t);
     for (int j = 0; j < nstep; ++j) {
       int nb;
@@ -436,7 +435,6 @@ __device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
       tc_commit(bar(s, B_PVDONE0 + pb));
       vr.next(nv);
       pr.next(2);
-      if (online && j + 1 < nstep) tc_commit(bar(s, B_OBAR));
     }
     tc_commit(bar(s, B_OFULL));
   }
@@ -536,7 +534,7 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
   const float c = p.scale_log2;
   const uint64_t c2 = f2_pack(c, c);
   const int n_items = p.n_tiles * p.bh;
-  uint32_t qc = 0, oc = 0, tiles_done = 0, xpar = 0, xc = 0;
+  uint32_t qc = 0, tiles_done = 0, xpar = 0, xc = 0;
   uint32_t su = 0;  // parity of the current use of S
   Ring pr;          // P buffer
 
@@ -616,8 +614,13 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
 #pragma unroll
         for (int v = 0; v < kNumWG; ++v) mall = fmaxf(mall, s.xch_m[(xpar * kNumWG + v) * kTileM + r]);
         xpar ^= 1u;
-        const float m_new = fmaxf(m, mall * c);
-        const float alpha = ex2_approx(m - m_new);
+        // Lazy rescale: the running max moves only when the step's max
+        // exceeds it by more than kLazyMax (log2 units), so p <= 2^kLazyMax
+        // (exact enough in fp32 and bf16) and O and l are rescaled rarely;
+        // O / l is unchanged in exact arithmetic whatever max is used.
+        const float m_top = fmaxf(m, mall * c);
+        const float m_new = m_top > m + kLazyMax ? m_top : m;
+        const float alpha = m_new == m ? 1.f : ex2_approx(m - m_new);
         const uint32_t pb = pr.slot;
         if (!wait_warp(s, bar(s, B_PVDONE0 + pb), pr.phase ^ 1u)) return;
         tc_fence_after();
@@ -627,27 +630,29 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         const float2 a = f2_unpack(f2_add(sa2, sb2));
         l = l * alpha + (a.x + a.y);
         m = m_new;
-        if (j > 0) {
-          // O += P(j-1) V must have landed before it is rescaled.
-          if (!wait_warp(s, bar(s, B_OBAR), oc & 1u)) return;
-          ++oc;
+        if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
+          // O += P(j-1) V must have landed before O is rescaled: PV(j-1)
+          // read the other P buffer, whose PV-done barrier is at most one
+          // use behind (its next use needs P(j+1)), so one parity wait is
+          // exact.  Ring position of step j-1: the other slot, same phase
+          // when this slot is 1, flipped when it is 0.
+          const uint32_t prev_phase = pb == 1u ? pr.phase : pr.phase ^ 1u;
+          if (!wait_warp(s, bar(s, B_PVDONE0 + (pb ^ 1u)), prev_phase)) return;
           tc_fence_after();
-          if (__any_sync(0xffffffffu, alpha < 1.f)) {
-            const uint64_t a2 = f2_pack(alpha, alpha);
+          const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
-            for (int k = 0; k < nog; ++k) {
-              uint32_t ra[16];
-              tmem_ld16(lane + ocol + k * 16, ra);
-              tmem_wait_ld16(ra);
+          for (int k = 0; k < nog; ++k) {
+            uint32_t ra[16];
+            tmem_ld16(lane + ocol + k * 16, ra);
+            tmem_wait_ld16(ra);
 #pragma unroll
-              for (int i = 0; i < 8; ++i) {
-                const float2 o2 = f2_unpack(f2_mul(
-                    f2_pack(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1])), a2));
-                ra[2 * i] = __float_as_uint(o2.x);
-                ra[2 * i + 1] = __float_as_uint(o2.y);
-              }
-              tmem_st16(lane + ocol + k * 16, ra);
+            for (int i = 0; i < 8; ++i) {
+              const float2 o2 = f2_unpack(f2_mul(
+                  f2_pack(__uint_as_float(ra[2 * i]), __uint_as_float(ra[2 * i + 1])), a2));
+              ra[2 * i] = __float_as_uint(o2.x);
+              ra[2 * i + 1] = __float_as_uint(o2.y);
             }
+            tmem_st16(lane + ocol + k * 16, ra);
           }
         }
         tmem_wait_st();
@@ -749,7 +754,6 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
     mbar_init(bar(s, B_QFULL), 1);
     mbar_init(bar(s, B_QEMPTY), kSoftmaxWarps);
     mbar_init(bar(s, B_QTFULL), kSoftmaxWarps);
-    mbar_init(bar(s, B_OBAR), 1);
     mbar_init(bar(s, B_OFULL), 1);
     mbar_init(bar(s, B_SFULL), 1);
     mbar_init(bar(s, B_SEMPTY), kSoftmaxWarps);
