@@ -155,3 +155,45 @@ def test_prepare_without_gpu_fails_loudly():
     plan = fw.wsattn_plan(4, 48, 1, 1, 2, 64)
     dummy = ctypes.c_void_p(1 << 20)
     assert fw.raw_call("wsattn_prepare")(plan.handle, 1, dummy, dummy, None) == 6  # CUDA
+
+
+def test_produce_argument_errors_without_device_work():
+    # wsattn_produce checks every argument before any CUDA call
+    import frame_aligned_window_gb300 as fw
+    produce = fw.raw_call("wsattn_produce")
+    a = ctypes.c_void_p(1 << 20)            # aligned, never dereferenced
+    mis = ctypes.c_void_p((1 << 20) + 8)    # not 16-byte aligned
+    f = ctypes.c_float
+    plan = fw.wsattn_plan(4, 48, 1, 1, 2, 128)      # H * D = 256
+    ok_args = [plan.handle, 1, a, 256, a, a, a, f(1e-6), a, a, a, None]
+
+    def call(**over):
+        args = list(ok_args)
+        names = ["plan", "batch", "x", "c", "w", "cos", "sin", "eps", "q", "k", "v", "stream"]
+        for key, val in over.items():
+            args[names.index(key)] = val
+        return produce(*args)
+
+    assert call(batch=0) == 1
+    for key in ("x", "w", "cos", "sin", "q", "k", "v"):
+        assert call(**{key: None}) == 1, key
+        assert call(**{key: mis}) == 1, key
+    assert call(c=96) == 1            # not a multiple of 64
+    assert call(c=0) == 1
+    assert call(eps=f(-1.0)) == 1
+    assert call(eps=f(float("nan"))) == 1
+    assert call(eps=f(float("inf"))) == 1
+    assert call(plan=None) == 1
+    # H * D = 64 is not a multiple of 128
+    small = fw.wsattn_plan(4, 48, 1, 1, 1, 64)
+    assert produce(small.handle, 1, a, 64, a, a, a, f(1e-6), a, a, a, None) == 3
+
+
+def test_schedule_reader_errors():
+    import frame_aligned_window_gb300 as fw
+    plan = fw.wsattn_plan(4, 48, 1, 1, 2, 64)
+    get = fw.raw_call("wsattn_get_schedule")
+    buf = (ctypes.c_int32 * 4)()
+    assert get(plan.handle, 1, 2, buf, 4) == 1       # far too small
+    assert get(plan.handle, 1, 2, None, 1 << 20) == 1
+    assert get(None, 1, 2, buf, 4) == 1
