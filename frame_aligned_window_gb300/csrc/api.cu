@@ -42,7 +42,7 @@ struct wsattn_plan_s {
   void* prod_ws = nullptr;
   float* inv_rms = nullptr;    // [B * N]
   float* key_parts = nullptr;  // [BH, 4 * ceil(N / 128), D]
-  float* key_sums = nullptr;   // [BH, D]
+  float* key_sums = nullptr;   // [BH, kKeySumRows, D]
 };
 
 namespace {
@@ -212,7 +212,7 @@ int ensure_prod_workspace(wsattn_plan_s* p, int batch, cudaStream_t stream) {
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
   const size_t n_inv = up(sizeof(float) * batch * hp.N);
   const size_t n_parts = up(sizeof(float) * BH * nparts * hp.D);
-  const size_t n_sums = up(sizeof(float) * BH * hp.D);
+  const size_t n_sums = up(sizeof(float) * BH * wsattn::kKeySumRows * hp.D);
   if (p->prod_ws) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return WSATTN_ERR_CUDA;
     cudaFree(p->prod_ws);
@@ -274,7 +274,8 @@ void free_device(wsattn_plan_s* p) {
 }
 
 // Enqueues the statistics passes for q, k (global or window bounds); with
-// key_sums ([BH, D], from the producer) the key-sum pass is skipped.
+// key_sums ([BH, kKeySumRows, D], from the producer) the key-sum pass is
+// skipped.
 int enqueue_prepare(wsattn_plan_s* plan, int batch, const void* q, const void* k,
                     const float* key_sums, cudaStream_t s) {
   const HostPlan& hp = plan->hp;

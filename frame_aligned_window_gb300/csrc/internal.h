@@ -116,8 +116,9 @@ struct FrameWindow {
 
 // Enqueues the three prepare passes; returns a cudaError_t.  With `win`
 // non-null the chunks must be the frames and the row bounds use the
-// per-window key-norm maximum.  With `key_sums` non-null ([BH, D]: each
-// head's key column sums, from the producer) pass A is skipped.
+// per-window key-norm maximum.  With `key_sums` non-null ([BH,
+// kKeySumRows, D]: each head's key column sums in kKeySumRows partial rows,
+// from the producer) pass A is skipped.
 cudaError_t launch_prepare(const void* q, const void* k, int BH, int64_t N, int D, float scale,
                            float tau, const PrepBuffers& buf, const FrameWindow* win,
                            const float* key_sums, cudaStream_t stream);
@@ -161,6 +162,7 @@ cudaError_t launch_forward(const FwdParams& p, int D, int grid, size_t smem, cud
 // bf16, head-packed [B, H, N, D] stores, and per-32-row key column sums.
 constexpr int kProdTileM = 128;  // tokens per tile (one batch element)
 constexpr int kProdTileK = 64;   // model-dim slice per pipeline stage
+constexpr int kKeySumRows = 8;   // partial key-sum rows per head the producer hands to prepare
 struct ProdParams {
   CUtensorMap tm_x;       // x [B, N, C] bf16, 3-D {C, N, B}, box {64, 128, 1}, 128-byte swizzle
   CUtensorMap tm_w;       // W [3HD, C] bf16, 2-D, box {64, BN / 2}, 128-byte swizzle

@@ -333,9 +333,9 @@ cudaError_t launch_prepare(const void* q, const void* k, int BH, int64_t N, int 
   const dim3 grid(b.nchunk, BH);
   const uint16_t* q16 = static_cast<const uint16_t*>(q);
   const uint16_t* k16 = static_cast<const uint16_t*>(k);
-  // key column sums: pass A's per-chunk sums, or one row per head given
+  // key column sums: pass A's per-chunk sums, or the producer's partial rows
   const float* sums = key_sums ? key_sums : b.part_sum;
-  const int nsum = key_sums ? 1 : b.nchunk;
+  const int nsum = key_sums ? kKeySumRows : b.nchunk;
   // every pass may start while its predecessor finishes and waits for it
   // on the device
   cudaError_t e = cudaSuccess;

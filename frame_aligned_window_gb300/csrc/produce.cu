@@ -404,11 +404,12 @@ __global__ void __launch_bounds__(256) rms_kernel(const uint16_t* __restrict__ x
   if (lane == 0) inv[row] = 1.0f / sqrtf(ss / static_cast<float>(C) + eps);
 }
 
-// Key column sums per head: the ordered sum of the epilogue's 32-row group
-// sums.  A CTA takes 32 columns of one head; thread (g, c) sums groups g,
-// g + 16, ... into eight interleaved accumulators (independent loads in
-// flight), then the accumulators and the 16 thread rows combine in a fixed
-// order.
+// Key column sums per head: the epilogue's 32-row group sums reduced to
+// kKeySumRows partial rows (the statistics pass adds those in order).  CTA
+// (x, bh, z) takes 32 columns of one head and the z-th share of its groups;
+// thread (g, c) sums groups g, g + 16, ... of the share into eight
+// interleaved accumulators (independent loads in flight), then the
+// accumulators and the 16 thread rows combine in a fixed order.
 constexpr int kRedRows = 16;
 __global__ void __launch_bounds__(32 * kRedRows) reduce_key_sums(const float* __restrict__ parts,
                                                                  int nparts, int D,
@@ -416,16 +417,19 @@ __global__ void __launch_bounds__(32 * kRedRows) reduce_key_sums(const float* __
   __shared__ float red[kRedRows][32];
   griddep_wait();  // the group sums come from the GEMM's epilogue
   const int bh = blockIdx.y, c = 32 * blockIdx.x + threadIdx.x, g = threadIdx.y;
+  const int per = (nparts + kKeySumRows - 1) / kKeySumRows;
+  const int p0 = static_cast<int>(blockIdx.z) * per;
+  const int p1 = min(nparts, p0 + per);
   const float* src = parts + static_cast<size_t>(bh) * nparts * D + c;
   float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
-  int i = g;
-  for (; i + 7 * kRedRows < nparts; i += 8 * kRedRows) {
+  int i = p0 + g;
+  for (; i + 7 * kRedRows < p1; i += 8 * kRedRows) {
 #pragma unroll
     for (int u = 0; u < 8; ++u) acc[u] += src[static_cast<size_t>(i + kRedRows * u) * D];
   }
 #pragma unroll
   for (int u = 0; u < 8; ++u)
-    if (i + kRedRows * u < nparts) acc[u] += src[static_cast<size_t>(i + kRedRows * u) * D];
+    if (i + kRedRows * u < p1) acc[u] += src[static_cast<size_t>(i + kRedRows * u) * D];
   float sum = 0.f;
 #pragma unroll
   for (int u = 0; u < 8; ++u) sum += acc[u];
@@ -434,7 +438,7 @@ __global__ void __launch_bounds__(32 * kRedRows) reduce_key_sums(const float* __
   if (g == 0) {
     float t = 0.f;
     for (int r = 0; r < kRedRows; ++r) t += red[r][threadIdx.x];
-    out[static_cast<size_t>(bh) * D + c] = t;
+    out[(static_cast<size_t>(bh) * kKeySumRows + blockIdx.z) * D + c] = t;
   }
 }
 
@@ -510,7 +514,8 @@ cudaError_t launch_produce(const ProdParams& p, const uint16_t* x, float eps, in
     e = bn == 256 ? launch_gemm<64, 256>(p, grid, stream) : launch_gemm<64, 128>(p, grid, stream);
   if (e != cudaSuccess) return e;
   const int BH = p.batch * p.heads;
-  return launch_dependent(reduce_key_sums, dim3(D / 32, BH), dim3(32, kRedRows), 0, stream,
+  return launch_dependent(reduce_key_sums, dim3(D / 32, BH, kKeySumRows), dim3(32, kRedRows), 0,
+                          stream,
                           static_cast<const float*>(p.part_sum), p.nparts, D, key_sums);
 }
 
