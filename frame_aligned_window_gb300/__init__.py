@@ -10,8 +10,7 @@ The names mirror the C ABI:
     wsattn_plan, wsattn_plan_ex, wsattn_plan_destroy, wsattn_prepare, wsattn_forward,
     wsattn_plan_info, wsattn_get_block_map, wsattn_get_csr, wsattn_get_stats,
     wsattn_plan_set_debug, wsattn_plan_set_bound, wsattn_device_status,
-    wsattn_selftest_timeout, wsattn_status_string, wsattn_prepare_static, wsattn_produce,
-    wsattn_get_schedule
+    wsattn_selftest_timeout, wsattn_status_string, wsattn_prepare_static, wsattn_produce
 """
 from __future__ import annotations
 
@@ -29,7 +28,7 @@ EXPORTS = (
     "wsattn_plan_info", "wsattn_get_block_map", "wsattn_get_csr", "wsattn_get_stats",
     "wsattn_plan_set_debug", "wsattn_plan_set_bound", "wsattn_device_status",
     "wsattn_selftest_timeout", "wsattn_status_string", "wsattn_prepare_static",
-    "wsattn_produce", "wsattn_get_schedule",
+    "wsattn_produce",
 )
 
 # wsattn_bound
@@ -73,7 +72,6 @@ _lib.wsattn_selftest_timeout.argtypes = [_I, ctypes.POINTER(_I), _P]
 _lib.wsattn_status_string.argtypes = [_I]
 _lib.wsattn_prepare_static.argtypes = [_I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P]
 _lib.wsattn_produce.argtypes = [_P, _I, _P, _I, _P, _P, _P, _F, _P, _P, _P, _P]
-_lib.wsattn_get_schedule.argtypes = [_P, _I, _I, _P, _SZ]
 _lib.wsattn_status_string.restype = ctypes.c_char_p
 for _name in EXPORTS:
     if _name != "wsattn_status_string":
@@ -267,16 +265,6 @@ def wsattn_get_stats(plan: Plan, batch: int, stream=None) -> dict:
                                  kmax.ctypes.data, bmax.ctypes.data, elig.ctypes.data,
                                  _stream_ptr(stream)), "wsattn_get_stats")
     return {"b": b, "m": m, "mu": mu, "kmax": kmax, "bmax": bmax, "elig": elig}
-
-
-def wsattn_get_schedule(plan: Plan, batch: int, grid: int) -> list:
-    """The forward's work lists: one list of work items per CTA."""
-    n_items = plan.tiles_per_head * batch * plan.heads
-    buf = np.zeros(grid + 1 + n_items, dtype=np.int32)
-    _check(_lib.wsattn_get_schedule(plan.handle, int(batch), int(grid), buf.ctypes.data,
-                                    buf.size), "wsattn_get_schedule")
-    ptr, items = buf[:grid + 1], buf[grid + 1:]
-    return [items[ptr[c]:ptr[c + 1]].tolist() for c in range(grid)]
 
 
 def wsattn_plan_set_debug(plan: Plan, force_path: int = -1, tau: float = 0.0):

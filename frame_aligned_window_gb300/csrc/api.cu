@@ -25,6 +25,7 @@ struct wsattn_plan_s {
   WorkTile* d_tiles = nullptr;
   int32_t* d_cls = nullptr;
   int* d_status = nullptr;
+  int* d_work = nullptr;  // the forward's work counters (zero between launches)
   // statistics workspace, sized for ws_batch
   int ws_batch = 0;
   void* ws = nullptr;
@@ -33,10 +34,6 @@ struct wsattn_plan_s {
   int force_path = -1;
   float tau = wsattn::kDefaultTau;
   int bound_mode = WSATTN_BOUND_GLOBAL;
-  // forward work schedule for (sched_bh, sched_grid)
-  int32_t* d_sched = nullptr;
-  size_t sched_cap = 0;  // int32 entries allocated
-  int sched_bh = 0, sched_grid = 0;
   // producer workspace (inverse RMS per token, key sums), sized for prod_batch
   int prod_batch = 0;
   void* prod_ws = nullptr;
@@ -136,12 +133,14 @@ int ensure_device(wsattn_plan_s* p) {
   const size_t cls_bytes = hp.cls.size() * sizeof(int32_t);
   if (cudaMalloc(&p->d_tiles, tiles_bytes) != cudaSuccess ||
       cudaMalloc(&p->d_cls, cls_bytes) != cudaSuccess ||
-      cudaMalloc(&p->d_status, sizeof(int)) != cudaSuccess)
+      cudaMalloc(&p->d_status, sizeof(int)) != cudaSuccess ||
+      cudaMalloc(&p->d_work, 2 * sizeof(int)) != cudaSuccess)
     return WSATTN_ERR_CUDA;
   if (cudaMemcpy(p->d_tiles, hp.tiles.data(), tiles_bytes, cudaMemcpyHostToDevice) !=
           cudaSuccess ||
       cudaMemcpy(p->d_cls, hp.cls.data(), cls_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
-      cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess)
+      cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess ||
+      cudaMemset(p->d_work, 0, 2 * sizeof(int)) != cudaSuccess)
     return WSATTN_ERR_CUDA;
   p->device = dev;
   p->num_sms = sms;
@@ -231,45 +230,18 @@ int ensure_prod_workspace(wsattn_plan_s* p, int batch, cudaStream_t stream) {
   return WSATTN_OK;
 }
 
-// The forward's per-CTA work lists for BH heads on `grid` CTAs (host-built
-// once per batch size; the upload synchronises the stream).
-int ensure_schedule(wsattn_plan_s* p, int BH, int grid, cudaStream_t stream) {
-  if (p->d_sched && p->sched_bh == BH && p->sched_grid == grid) return WSATTN_OK;
-  std::vector<int32_t> h;
-  try {
-    h = wsattn::build_schedule(p->hp, BH, grid);
-  } catch (const std::bad_alloc&) {
-    return WSATTN_ERR_NO_MEMORY;
-  }
-  if (cudaStreamSynchronize(stream) != cudaSuccess) return WSATTN_ERR_CUDA;
-  if (h.size() > p->sched_cap) {
-    if (p->d_sched) cudaFree(p->d_sched);
-    p->d_sched = nullptr;
-    p->sched_cap = 0;
-    if (cudaMalloc(&p->d_sched, h.size() * sizeof(int32_t)) != cudaSuccess) return WSATTN_ERR_CUDA;
-    p->sched_cap = h.size();
-  }
-  if (cudaMemcpy(p->d_sched, h.data(), h.size() * sizeof(int32_t), cudaMemcpyHostToDevice) !=
-      cudaSuccess)
-    return WSATTN_ERR_CUDA;
-  p->sched_bh = BH;
-  p->sched_grid = grid;
-  return WSATTN_OK;
-}
-
 void free_device(wsattn_plan_s* p) {
   if (p->prod_ws) cudaFree(p->prod_ws);
   p->prod_ws = nullptr;
-  if (p->d_sched) cudaFree(p->d_sched);
-  p->d_sched = nullptr;
-  p->sched_cap = 0;
   if (p->d_tiles) cudaFree(p->d_tiles);
   if (p->d_cls) cudaFree(p->d_cls);
   if (p->d_status) cudaFree(p->d_status);
+  if (p->d_work) cudaFree(p->d_work);
   if (p->ws) cudaFree(p->ws);
   p->d_tiles = nullptr;
   p->d_cls = nullptr;
   p->d_status = nullptr;
+  p->d_work = nullptr;
   p->ws = nullptr;
 }
 
@@ -447,9 +419,7 @@ int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, 
   if (prm.stages_k < 2 || smem > plan->smem_optin) return WSATTN_ERR_UNSUPPORTED;
   const int64_t items = static_cast<int64_t>(prm.n_tiles) * BH;
   const int grid = static_cast<int>(items < plan->num_sms ? items : plan->num_sms);
-  rc = ensure_schedule(plan, BH, grid, static_cast<cudaStream_t>(stream));
-  if (rc != WSATTN_OK) return rc;
-  prm.sched = plan->d_sched;
+  prm.work = plan->d_work;
   if (wsattn::launch_forward(prm, hp.D, grid, smem, static_cast<cudaStream_t>(stream)) !=
       cudaSuccess)
     return WSATTN_ERR_CUDA;
@@ -476,21 +446,6 @@ int wsattn_plan_info(wsattn_plan_t plan, int64_t* info, int n) {
 int wsattn_get_block_map(wsattn_plan_t plan, uint8_t* host, size_t n) {
   if (!plan || !host || n < plan->hp.bitmap.size()) return WSATTN_ERR_BAD_ARG;
   std::memcpy(host, plan->hp.bitmap.data(), plan->hp.bitmap.size());
-  return WSATTN_OK;
-}
-
-int wsattn_get_schedule(wsattn_plan_t plan, int batch, int grid, int32_t* host, size_t n) {
-  if (!plan || !host || batch < 1 || grid < 1) return WSATTN_ERR_BAD_ARG;
-  const int64_t BH = static_cast<int64_t>(batch) * plan->hp.H;
-  const int64_t need = grid + 1 + static_cast<int64_t>(plan->hp.tiles.size()) * BH;
-  if (BH >= (int64_t(1) << 31) || need >= (int64_t(1) << 31) || n < static_cast<size_t>(need))
-    return WSATTN_ERR_BAD_ARG;
-  try {
-    const std::vector<int32_t> v = wsattn::build_schedule(plan->hp, static_cast<int>(BH), grid);
-    std::memcpy(host, v.data(), v.size() * sizeof(int32_t));
-  } catch (const std::bad_alloc&) {
-    return WSATTN_ERR_NO_MEMORY;
-  }
   return WSATTN_OK;
 }
 

@@ -42,9 +42,13 @@
 //
 // Work items (tile, b*h) are ordered class by class (tiles with equal key
 // lists, longest first) and head by head inside a class, so the CTAs running
-// at one time stream the same head's keys and values through L2; the host
-// deals that list out longest-processing-time first (build_schedule) and
-// every role of a CTA walks the CTA's own list.  The kernel is a dependent
+// at one time stream the same head's keys and values through L2.  They are
+// dealt out on the device: a CTA's TMA warp takes the next index from a
+// global counter when it starts on an item and passes it to the CTA's other
+// roles through a small queue in shared memory, so the items go to whichever
+// CTA is free first (list scheduling in the longest-first order) and the
+// deal adapts to the actual cost of each item (online heads are slower).
+// The last CTA to finish resets the counter.  The kernel is a dependent
 // launch: its prologue overlaps the end of the statistics pass before it.
 //
 // Every wait is bounded: on expiry the kernel sets a bit in the status word,
@@ -70,6 +74,11 @@ constexpr long long kWaitLimitCycles = 1LL << 31;  // about one second
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr float kLazyMax = 8.f;  // online path: rescale when the max grows by > 2^8
 constexpr uint32_t kTmemCols = 512;
+// Work items are dealt out on the device: the TMA warp takes the next index
+// from a global counter and passes it to the CTA's other roles through a
+// small queue in shared memory.
+constexpr int kItemQueue = 4;
+constexpr uint32_t kItemReaders = 2 + kSoftmaxWarps;  // both issuers and every softmax warp
 
 // mbarrier slots
 enum : int {
@@ -88,7 +97,9 @@ enum : int {
   B_KEMPTY0 = B_KFULL0 + 4,
   B_VFULL0 = B_KEMPTY0 + 4,
   B_VEMPTY0 = B_VFULL0 + 4,
-  B_COUNT = B_VEMPTY0 + 4
+  B_IQFULL0 = B_VEMPTY0 + 4,     // TMA warp -> the other roles: work item in queue slot
+  B_IQEMPTY0 = B_IQFULL0 + kItemQueue,  // every role has read the slot
+  B_COUNT = B_IQEMPTY0 + kItemQueue
 };
 // Exchange area after the barriers: row maxima and row sums of the
 // warpgroups, double-buffered: float [2 parity][kNumWG][128 rows] each.
@@ -103,6 +114,7 @@ struct Shared {
   uint32_t q, k, v, bars;  // shared-window addresses
   uint32_t ostage;         // epilogue staging chunks (kOChunkBytes per softmax warp)
   float* xch_m;            // [2][kNumWG][128]
+  volatile int32_t* iq;    // [kItemQueue] work items (-1: no more)
   float* xch_l;            // [2][kNumWG][128]
   volatile int* abort_flag;
   int* status;
@@ -137,6 +149,17 @@ __device__ __forceinline__ bool wait_warp(const Shared& s, uint32_t b, uint32_t 
   return __all_sync(0xffffffffu, ok);
 }
 
+// Position in the work-item queue.
+struct ItemPos {
+  uint32_t slot = 0, phase = 0;
+  __device__ __forceinline__ void next() {
+    if (++slot == kItemQueue) {
+      slot = 0;
+      phase ^= 1u;
+    }
+  }
+};
+
 // Arrival of one softmax warp: the warp's threads synchronise (ordering
 // every lane's prior shared-memory writes and fenced tcgen05 operations
 // before it) and lane 0 arrives.  Barriers the softmax warps signal count
@@ -146,6 +169,38 @@ __device__ __forceinline__ bool wait_warp(const Shared& s, uint32_t b, uint32_t 
 __device__ __forceinline__ void warp_arrive(uint32_t b) {
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(b);
+}
+
+// TMA warp: takes the next work item from the launch's counter and posts it
+// to the queue.  Returns the item, -1 once none is left (posted too, so the
+// other roles stop), -2 on an expired wait.
+__device__ __forceinline__ int post_item(const FwdParams& p, const Shared& s, ItemPos& q,
+                                         int n_items) {
+  if (!wait(s, bar(s, B_IQEMPTY0 + q.slot), q.phase ^ 1u, kStatusTimeoutProducer)) return -2;
+  int it = atomicAdd(p.work, 1);
+  if (it >= n_items) it = -1;
+  s.iq[q.slot] = it;
+  mbar_arrive(bar(s, B_IQFULL0 + q.slot));
+  q.next();
+  return it;
+}
+
+// An issuer thread's next work item (-1: none left, -2: expired wait).
+__device__ __forceinline__ int read_item(const Shared& s, ItemPos& q, int code) {
+  if (!wait(s, bar(s, B_IQFULL0 + q.slot), q.phase, code)) return -2;
+  const int it = s.iq[q.slot];
+  mbar_arrive(bar(s, B_IQEMPTY0 + q.slot));
+  q.next();
+  return it;
+}
+
+// A softmax warp's next work item (warp-uniform; one arrival per warp).
+__device__ __forceinline__ int read_item_warp(const Shared& s, ItemPos& q) {
+  if (!wait_warp(s, bar(s, B_IQFULL0 + q.slot), q.phase)) return -2;
+  const int it = s.iq[q.slot];
+  warp_arrive(bar(s, B_IQEMPTY0 + q.slot));
+  q.next();
+  return it;
 }
 
 // Barrier of the two softmax warpgroups (every warp arrives, then waits for
@@ -195,19 +250,6 @@ __device__ __forceinline__ Item map_item(const FwdParams& p, int it) {
   const int o = it - p.bh * beg;
   return Item{beg + o % n, o / n};
 }
-
-// This CTA's work items in order, from the host-built schedule (every role
-// of the CTA walks the same list).
-struct WorkList {
-  const int32_t* items;
-  int n;
-  __device__ __forceinline__ explicit WorkList(const FwdParams& p) {
-    const int b = __ldg(p.sched + blockIdx.x), e = __ldg(p.sched + blockIdx.x + 1);
-    items = p.sched + gridDim.x + 1 + b;
-    n = e - b;
-  }
-  __device__ __forceinline__ int operator[](int k) const { return __ldg(items + k); }
-};
 
 // Position in a ring of `n` stages: slot and the parity of its current use.
 // Advanced by increments only (no division in the per-step loops).
@@ -281,9 +323,12 @@ __device__ void producer(const FwdParams& p, const Shared& s) {
     drain_loads(bar(s, B_VFULL0), static_cast<int>(nv), vph, viss);
     drain_loads(bar(s, B_QFULL), 1, (qc - 1u) & 1u, qc > 0 ? 1u : 0u);
   };
-  const WorkList wl(p);
-  for (int w = 0; w < wl.n; ++w) {
-    const int it = wl[w];
+  const int n_items = p.n_tiles * p.bh;
+  ItemPos iq;
+  while (true) {
+    const int it = post_item(p, s, iq, n_items);
+    if (it == -2) return drain();
+    if (it < 0) break;
     const Item im = map_item(p, it);
     const WorkTile t = p.tiles[im.tile];
     const int y0 = im.bh * p.n;
@@ -358,9 +403,10 @@ __device__ void qk_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
   uint32_t su = 0;  // parity of the current use of S
   uint32_t tiles_done = 0;
   Steps qs;
-  const WorkList wl(p);
-  for (int w = 0; w < wl.n; ++w) {
-    const int it = wl[w];
+  ItemPos iq;
+  while (true) {
+    const int it = read_item(s, iq, kStatusTimeoutMma);
+    if (it < 0) break;
     const Item im = map_item(p, it);
     const WorkTile t = p.tiles[im.tile];
     qs.init(t);
@@ -407,9 +453,10 @@ __device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
   const uint32_t nv = static_cast<uint32_t>(p.stages_v);
   Ring vr, pr;
   Steps ps;
-  const WorkList wl(p);
-  for (int w = 0; w < wl.n; ++w) {
-    const int it = wl[w];
+  ItemPos iq;
+  while (true) {
+    const int it = read_item(s, iq, kStatusTimeoutMma);
+    if (it < 0) break;
     const Item im = map_item(p, it);
     const WorkTile t = p.tiles[im.tile];
     const int nstep = t.nstep;
@@ -533,14 +580,13 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
   const uint32_t ocol = tc_.o + static_cast<uint32_t>(16 * og0);
   const float c = p.scale_log2;
   const uint64_t c2 = f2_pack(c, c);
-  const int n_items = p.n_tiles * p.bh;
   uint32_t qc = 0, tiles_done = 0, xpar = 0, xc = 0;
   uint32_t su = 0;  // parity of the current use of S
   Ring pr;          // P buffer
 
-  const WorkList wl(p);
-  if (wl.n == 0) return;
-  int w = 0, it = wl[0];
+  ItemPos iq;
+  int it = read_item_warp(s, iq);
+  if (it < 0) return;
   if (!load_q<D>(s, lane + tc_.q, wg, r, p.tiles[map_item(p, it).tile].nvalid, qc)) return;
   while (true) {
     const Item im = map_item(p, it);
@@ -663,8 +709,9 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
     }
 
     // Stage the next tile's Q so its first QK products overlap this epilogue.
-    const int nxt = w + 1 < wl.n ? wl[w + 1] : n_items;
-    if (nxt < n_items &&
+    const int nxt = read_item_warp(s, iq);
+    if (nxt == -2) return;
+    if (nxt >= 0 &&
         !load_q<D>(s, lane + tc_.q, wg, r, p.tiles[map_item(p, nxt).tile].nvalid, qc))
       return;
 
@@ -722,9 +769,8 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
                                __uint_as_float(v[4 * i + 3]) * inv);
       }
     }
-    if (nxt >= n_items) break;
+    if (nxt < 0) break;
     it = nxt;
-    ++w;
   }
 }
 
@@ -744,7 +790,8 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
   uint8_t* gbars = smem_raw + (s.bars - raw);
   s.xch_m = reinterpret_cast<float*>(gbars + 8 * B_COUNT + 16);
   s.xch_l = s.xch_m + 2 * kNumWG * kTileM;
-  s.ostage = (s.bars + 8u * B_COUNT + 16u + kXchBytes + 511u) & ~511u;
+  s.iq = reinterpret_cast<volatile int32_t*>(s.xch_l + 2 * kNumWG * kTileM);
+  s.ostage = (s.bars + 8u * B_COUNT + 16u + kXchBytes + 4u * kItemQueue + 511u) & ~511u;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(gbars + 8 * B_COUNT);
   s.abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   s.status = p.status;
@@ -767,6 +814,10 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
       mbar_init(bar(s, B_KEMPTY0 + i), 1);
       mbar_init(bar(s, B_VFULL0 + i), 1);
       mbar_init(bar(s, B_VEMPTY0 + i), 1);
+    }
+    for (int i = 0; i < kItemQueue; ++i) {
+      mbar_init(bar(s, B_IQFULL0 + i), 1);
+      mbar_init(bar(s, B_IQEMPTY0 + i), kItemReaders);
     }
     *s.abort_flag = 0;
     fence_barrier_init();
@@ -803,6 +854,16 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
   __syncthreads();
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tbase, kTmemCols);
+  // The last CTA to finish (every CTA has drawn its last item by now) resets
+  // the work counter for the next launch.
+  if (threadIdx.x == 0) {
+    __threadfence();
+    if (atomicAdd(p.work + 1, 1) == static_cast<int>(gridDim.x) - 1) {
+      p.work[0] = 0;
+      p.work[1] = 0;
+      __threadfence();
+    }
+  }
 }
 
 __global__ void timeout_selftest_kernel(long long limit_cycles, int* status) {
@@ -861,7 +922,7 @@ cudaError_t launch_d(const FwdParams& p, int grid, size_t smem, cudaStream_t str
 size_t forward_smem_bytes(int D, int step_keys, int stages_k, int stages_v) {
   const size_t stage = static_cast<size_t>(step_keys) * D * 2;
   return 1024 + static_cast<size_t>(kTileM) * D * 2 + (stages_k + stages_v) * stage +
-         8 * B_COUNT + 16 + kXchBytes + 512 + kOStageBytes;
+         8 * B_COUNT + 16 + kXchBytes + 4 * kItemQueue + 512 + kOStageBytes;
 }
 
 void forward_stages(int D, int step_keys, size_t smem_optin, int* stages_k, int* stages_v) {

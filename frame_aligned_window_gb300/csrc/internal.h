@@ -78,12 +78,6 @@ __host__ __device__ inline bool frames_interact(int a, int c, int F, int w, int 
   return (d < 0 ? -d : d) <= w;
 }
 
-// Forward work schedule for BH heads on `grid` CTAs: work items (in the
-// kernel's item order) dealt out longest-processing-time first, each to the
-// CTA with the least predicted work so far.  Returns grid + 1 list offsets
-// followed by the items of CTA 0, CTA 1, ... (each list in item order).
-std::vector<int32_t> build_schedule(const HostPlan& hp, int BH, int grid);
-
 // Picks a block size for T: among the valid sizes (multiples of 16 dividing
 // T, at most kStepKeys), the one whose forward key step
 // floor(kStepKeys / bk) * bk is longest, the larger on ties.
@@ -134,7 +128,7 @@ struct FwdParams {
   CUtensorMap tm_o;  // [BH*N, D] fp32, box {16, 32}, no swizzle (epilogue stores)
   const WorkTile* tiles;
   const int32_t* cls;    // class boundaries into tiles, n_cls + 1 entries
-  const int32_t* sched;  // build_schedule(): gridDim.x + 1 offsets, then the CTAs' items
+  int* work;             // [2]: next work item, CTAs finished (both 0 between launches)
   int n_cls;
   const float* m_rows;   // [BH*N] fixed softmax max per row (uncentered logit units)
   const uint8_t* elig;   // [BH]

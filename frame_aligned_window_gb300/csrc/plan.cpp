@@ -16,10 +16,6 @@
 #include <algorithm>
 #include <new>
 
-#include <functional>
-#include <queue>
-#include <utility>
-
 #include "internal.h"
 
 namespace wsattn {
@@ -144,39 +140,6 @@ int build_host_plan(int frames, int tokens_per_frame, int window, int ref_frames
     return WSATTN_ERR_NO_MEMORY;
   }
   return WSATTN_OK;
-}
-
-std::vector<int32_t> build_schedule(const HostPlan& hp, int BH, int grid) {
-  // Predicted cost of a work tile, in units of 100 cycles: about 1600
-  // cycles per key step and 3500 per tile (Q staging, epilogue).
-  constexpr int64_t kStepCost = 16, kTileCost = 35;
-  const int n_cls = static_cast<int>(hp.cls.size()) - 1;
-  const int64_t n_items = static_cast<int64_t>(hp.tiles.size()) * BH;
-  std::vector<int32_t> owner(static_cast<size_t>(n_items));
-  std::vector<int32_t> count(static_cast<size_t>(grid), 0);
-  // least-loaded CTA first, the lower index on ties
-  using Slot = std::pair<int64_t, int32_t>;
-  std::priority_queue<Slot, std::vector<Slot>, std::greater<Slot>> heap;
-  for (int32_t c = 0; c < grid; ++c) heap.push({0, c});
-  int64_t it = 0;
-  for (int c = 0; c < n_cls; ++c) {  // the kernel's item order: class, head, tile
-    const int32_t beg = hp.cls[c], n = hp.cls[c + 1] - beg;
-    for (int64_t o = 0; o < static_cast<int64_t>(n) * BH; ++o, ++it) {
-      const WorkTile& t = hp.tiles[beg + o % n];
-      const Slot sl = heap.top();
-      heap.pop();
-      owner[it] = sl.second;
-      ++count[sl.second];
-      heap.push({sl.first + kStepCost * t.nstep + kTileCost, sl.second});
-    }
-  }
-  std::vector<int32_t> out(static_cast<size_t>(grid) + 1 + static_cast<size_t>(n_items));
-  out[0] = 0;
-  for (int c = 0; c < grid; ++c) out[c + 1] = out[c] + count[c];
-  std::vector<int32_t> fill(out.begin(), out.begin() + grid);
-  for (int64_t i = 0; i < n_items; ++i)
-    out[static_cast<size_t>(grid) + 1 + fill[owner[i]]++] = static_cast<int32_t>(i);
-  return out;
 }
 
 }  // namespace wsattn

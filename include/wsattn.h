@@ -28,8 +28,7 @@
  *   - `stream` is a cudaStream_t (NULL = legacy default stream); all device
  *     work is enqueued on it.  No call synchronises the host except the
  *     wsattn_get_* readers and wsattn_device_status, and the calls that grow
- *     a plan's workspace or build its forward schedule (the first call for a
- *     larger batch); each says so.
+ *     a plan's workspace (the first call for a larger batch); each says so.
  *   - Every call returns a status code (WSATTN_OK = 0 or one of the errors
  *     below) and never throws or aborts.  Argument errors are reported before
  *     any work is enqueued.  Asynchronous device errors (CUDA faults, expired
@@ -180,11 +179,10 @@ int wsattn_produce(wsattn_plan_t plan, int batch, const void* x, int model_dim,
  *   v    bf16 [batch, H, N, D]
  *   out  fp32 [batch, H, N, D], fully overwritten
  * Requires a prior wsattn_prepare on this plan with the same batch.
- * The first call for a batch size builds the kernel's work schedule on the
- * host (each CTA's list of query tiles, longest-processing-time first) and
- * uploads it, which synchronises `stream`; make it outside stream capture.
+ * Work items (a query tile of one head) are dealt out on the device, in
+ * order of decreasing key-list length, to whichever CTA is free first.
  * Errors: BAD_ARG, NOT_PREPARED, BATCH_MISMATCH, UNSUPPORTED (block_k > 160),
- *         NO_MEMORY, CUDA.
+ *         CUDA.
  */
 int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, const void* v,
                    float* out, void* stream);
@@ -230,16 +228,6 @@ int wsattn_plan_info(wsattn_plan_t plan, int64_t* info, int n);
 /* Copies the block bitmap (row-major [N/block_q, N/block_k], 1 = active)
  * into host memory of n bytes.  Errors: BAD_ARG if n is too small. */
 int wsattn_get_block_map(wsattn_plan_t plan, uint8_t* host, size_t n);
-
-/* Copies the forward's work schedule for `batch` on `grid` CTAs (host only;
- * wsattn_forward launches min(#SMs, work items) CTAs): grid + 1 offsets,
- * then the work items of CTA 0, CTA 1, ... in order, n = grid + 1 +
- * tiles * batch * heads entries (tiles: wsattn_plan_info).  Work item i is
- * tile i mod (class size) of its class and head (b * heads + h) as the
- * kernel decodes it; items are dealt longest-processing-time first, each to
- * the CTA with the least predicted work.
- * Errors: BAD_ARG (batch or grid < 1, or n too small), NO_MEMORY. */
-int wsattn_get_schedule(wsattn_plan_t plan, int batch, int grid, int32_t* host, size_t n);
 
 /* Copies the CSR of active blocks: row_ptr[N/block_q + 1], col[nnz] (key
  * block indices, increasing within a row), into host arrays of the given

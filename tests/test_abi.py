@@ -187,13 +187,3 @@ def test_produce_argument_errors_without_device_work():
     # H * D = 64 is not a multiple of 128
     small = fw.wsattn_plan(4, 48, 1, 1, 1, 64)
     assert produce(small.handle, 1, a, 64, a, a, a, f(1e-6), a, a, a, None) == 3
-
-
-def test_schedule_reader_errors():
-    import frame_aligned_window_gb300 as fw
-    plan = fw.wsattn_plan(4, 48, 1, 1, 2, 64)
-    get = fw.raw_call("wsattn_get_schedule")
-    buf = (ctypes.c_int32 * 4)()
-    assert get(plan.handle, 1, 2, buf, 4) == 1       # far too small
-    assert get(plan.handle, 1, 2, None, 1 << 20) == 1
-    assert get(None, 1, 2, buf, 4) == 1
