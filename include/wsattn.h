@@ -180,7 +180,9 @@ int wsattn_produce(wsattn_plan_t plan, int batch, const void* x, int model_dim,
  *   out  fp32 [batch, H, N, D], fully overwritten
  * Requires a prior wsattn_prepare on this plan with the same batch.
  * Work items (a query tile of one head) are dealt out on the device, in
- * order of decreasing key-list length, to whichever CTA is free first.
+ * order of decreasing key-list length, to whichever CTA is free first, from
+ * a counter the plan owns: two forwards of one plan must not run at the
+ * same time on the device (on different streams without ordering).
  * Errors: BAD_ARG, NOT_PREPARED, BATCH_MISMATCH, UNSUPPORTED (block_k > 160),
  *         CUDA.
  */
