@@ -150,3 +150,19 @@ def test_inputs_recipe_shapes_and_table():
     assert c.shape == (wl.n_tokens, 32) and c.dtype == torch.float32
     np.testing.assert_allclose((c.double() ** 2 + s.double() ** 2).numpy(), 1.0, atol=1e-6)
     assert torch.all(c[0] == 1) and torch.all(s[0] == 0)  # token 0: frame, row, col 0
+
+
+def test_rope_table_decomposes_positions():
+    # token -> (frame, row, column) of a frame's latent grid, each group of
+    # dimension pairs turning by position * base^(-j / n)
+    T, gw, D = 40, 8, 64
+    c, s = workloads.rope_table(3 * T, T, gw, D)
+    half = D // 2
+    n_hw = half // 3
+    n_t = half - 2 * n_hw
+    tok = T + 2 * gw + 3                    # frame 1, row 2, column 3
+    want = ([1 * 10000.0 ** (-j / n_t) for j in range(n_t)]
+            + [2 * 10000.0 ** (-j / n_hw) for j in range(n_hw)]
+            + [3 * 10000.0 ** (-j / n_hw) for j in range(n_hw)])
+    np.testing.assert_allclose(c[tok].double().numpy(), np.cos(want), atol=1e-6)
+    np.testing.assert_allclose(s[tok].double().numpy(), np.sin(want), atol=1e-6)
