@@ -32,6 +32,11 @@
 //   warp 1  MMA issuer: 4 x tcgen05.mma M=128 N=BN K=16 per stage
 //   warp 2  TMEM allocation
 //   warps 4-7 epilogue: thread = token row (TMEM lane)
+// W is loaded evict-last (it is re-read for every token tile) and q, k, v
+// are stored evict-first.  The GEMM is a dependent launch after the RMS
+// pre-pass: its main loop reads only x and W, and only the epilogue waits
+// for the pre-pass's 1/rms values.  Every wait is bounded; after an expired
+// one the TMA producer waits (bounded) for its loads in flight.
 #include <cuda_bf16.h>
 
 #include "internal.h"
