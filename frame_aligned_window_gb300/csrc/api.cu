@@ -349,7 +349,7 @@ int wsattn_produce(wsattn_plan_t plan, int batch, const void* x, int model_dim,
   std::memset(&prm, 0, sizeof(prm));
   void* outs[3] = {q, k, v};
   if (!encode_x_map(&prm.tm_x, x, batch, hp.N, model_dim) ||
-      !encode_map(&prm.tm_w, w_qkv, 3LL * hp.H * hp.D, model_dim, bn / 2))
+      !encode_map(&prm.tm_w, w_qkv, 3LL * hp.H * hp.D, model_dim, bn))
     return WSATTN_ERR_CUDA;
   for (int i = 0; i < 3; ++i)
     if (!encode_head_map(&prm.tm_out[i], outs[i], BH, hp.N, hp.D)) return WSATTN_ERR_CUDA;
@@ -364,9 +364,8 @@ int wsattn_produce(wsattn_plan_t plan, int batch, const void* x, int model_dim,
   prm.c = model_dim;
   prm.mtiles = static_cast<int>((hp.N + wsattn::kProdTileM - 1) / wsattn::kProdTileM);
   prm.ntiles = 3 * hp.H * hp.D / bn;
-  prm.mpairs = (prm.mtiles + 1) / 2;
   prm.nparts = 4 * prm.mtiles;
-  const int grid = plan->num_sms;  // an upper bound: the launch sizes the cluster grid
+  const int grid = plan->num_sms;  // one CTA per SM at most
   if (wsattn::launch_produce(prm, static_cast<const uint16_t*>(x), eps, hp.D, bn, grid,
                              plan->inv_rms, plan->key_sums, s) != cudaSuccess)
     return WSATTN_ERR_CUDA;
@@ -510,7 +509,12 @@ int wsattn_device_status(wsattn_plan_t plan, void* stream) {
   if (cudaMemcpy(&st, plan->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return WSATTN_ERR_CUDA;
   if (st == 0) return WSATTN_OK;
-  if (cudaMemset(plan->d_status, 0, sizeof(int)) != cudaSuccess) return WSATTN_ERR_CUDA;
+  // A forward that gave up on a wait may leave its work counters non-zero
+  // (the last CTA to finish resets them); the next forward would then skip
+  // items.  Reset them with the status word.
+  if (cudaMemset(plan->d_status, 0, sizeof(int)) != cudaSuccess ||
+      (plan->d_work && cudaMemset(plan->d_work, 0, 2 * sizeof(int)) != cudaSuccess))
+    return WSATTN_ERR_CUDA;
   return WSATTN_ERR_TIMEOUT;
 }
 

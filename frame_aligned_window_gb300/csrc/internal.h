@@ -159,7 +159,7 @@ constexpr int kProdTileK = 64;   // model-dim slice per pipeline stage
 constexpr int kKeySumRows = 8;   // partial key-sum rows per head the producer hands to prepare
 struct ProdParams {
   CUtensorMap tm_x;       // x [B, N, C] bf16, 3-D {C, N, B}, box {64, 128, 1}, 128-byte swizzle
-  CUtensorMap tm_w;       // W [3HD, C] bf16, 2-D, box {64, BN / 2}, 128-byte swizzle
+  CUtensorMap tm_w;       // W [3HD, C] bf16, 2-D, box {64, BN}, 128-byte swizzle
   CUtensorMap tm_out[3];  // q, k, v [BH, N, D] bf16, 3-D {D, N, BH}, box {64, 32, 1}, swizzled
   const float* inv_rms;   // [B * N] 1 / sqrt(mean x^2 + eps)
   const float* rope_cos;  // [N, D / 2]
@@ -168,15 +168,13 @@ struct ProdParams {
   int* status;            // device status word (bit set on an expired wait)
   int batch, heads, n, c;
   int mtiles;             // ceil(N / 128)
-  int mpairs;             // ceil(mtiles / 2): token-tile pairs (one per CTA cluster)
   int ntiles;             // 3HD / BN
   int nparts;             // 4 * mtiles
 };
 // BN (feature columns per tile) for H * D, 0 if unsupported.
 int produce_tile_n(int heads, int head_dim);
 size_t produce_smem_bytes(int bn);
-// RMS pre-pass, the producer GEMM (clusters of two CTAs, at most `grid`
-// CTAs) and the reduction of the key column sums into [BH, D]; returns a
+// RMS pre-pass, the producer GEMM (persistent, at most `grid` CTAs) and the reduction of the key column sums into [BH, D]; returns a
 // cudaError_t.
 cudaError_t launch_produce(const ProdParams& p, const uint16_t* x, float eps, int D, int bn,
                            int grid, float* inv_rms, float* key_sums, cudaStream_t stream);

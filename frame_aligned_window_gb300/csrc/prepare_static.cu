@@ -8,7 +8,10 @@
 // cudaMalloc's implicit device synchronisation.  This entry point runs the
 // same three prepare kernels, writes the statistics into buffers the caller
 // passes in, and takes its scratch from a fixed array in the library's own
-// device image instead of allocating it.
+// device image instead of allocating it.  It takes no plan, so it always
+// uses the global bound (the maximum key norm over all keys of the head):
+// its results equal wsattn_prepare's on a plan left at the default bound;
+// window bounds (wsattn_plan_set_bound) and mask flags do not apply.
 //
 // The scratch array, g_prepare_scratch below, holds kStaticSlots chunk slots
 // (a partial key-column sum of up to 128 floats plus two partial maxima per
@@ -99,14 +102,10 @@ extern "C" int wsattn_prepare_static(int batch, int heads, int n_tokens, int hea
 
   int nchunk = 0, rpc = 0;
   prepare_chunking(BH, N, num_sms, &nchunk, &rpc);
-  if (static_cast<int64_t>(nchunk) * BH > kStaticSlots) {
-    // fewer, longer chunks so that every (b, h) fits in the slots
-    const int64_t max_chunks = kStaticSlots / BH;
-    int64_t r = (N + max_chunks - 1) / max_chunks;
-    r = (r + 15) / 16 * 16;
-    rpc = static_cast<int>(r);
-    nchunk = static_cast<int>((N + r - 1) / r);
-  }
+  // prepare_chunking gives at most max(BH, 3 * SMs) chunks in all, so this
+  // holds on every GPU with fewer than 683 SMs; refuse rather than overrun
+  // the scratch if the chunking ever asks for more.
+  if (static_cast<int64_t>(nchunk) * BH > kStaticSlots) return WSATTN_ERR_BAD_ARG;
 
   PrepBuffers b;
   b.b_rows = b_rows;

@@ -23,12 +23,9 @@
 // Kernel shape (one CTA per SM, persistent): tiles of 128 tokens x BN
 // features (BN = 256, or 128 when H * D is not a multiple of 256), 64-wide
 // model-dim stages in a 4-deep TMA ring, two TMEM accumulators so the MMA of
-// one tile overlaps the epilogue of the previous one.  CTAs run in clusters
-// of two that take the two token tiles of one feature tile: each CTA loads
-// its own x tile and half of the W tile, multicast into both CTAs, so a
-// stage costs 32 KB of L2 traffic per CTA instead of 48 KB (a stage slot is
-// refilled only when both CTAs' MMAs have released it).
-//   warp 0  TMA producer (x tile 128 x 64, half the W tile BN/2 x 64)
+// one tile overlaps the epilogue of the previous one.  Each CTA loads its
+// own x tile and W tile for every stage.
+//   warp 0  TMA producer (x tile 128 x 64, W tile BN x 64)
 //   warp 1  MMA issuer: 4 x tcgen05.mma M=128 N=BN K=16 per stage
 //   warp 2  TMEM allocation
 //   warps 4-7 epilogue: thread = token row (TMEM lane)
@@ -96,23 +93,21 @@ struct PTile {
   int b, mt, nt;
 };
 
-// Work unit t of a cluster: feature tile nt of token tiles 2 mp and 2 mp + 1
-// of batch element b; this CTA takes token tile 2 mp + rank (which is past
-// the last tile when mtiles is odd: its rows read as zero and store nothing).
-__device__ __forceinline__ PTile decode(const ProdParams& p, int t, uint32_t rank) {
+// Work unit t: feature tile nt of token tile mt of batch element b, token
+// tile major (the feature tiles of one x slice are consecutive units, so the
+// CTAs running at one time share that slice in L2).
+__device__ __forceinline__ PTile decode(const ProdParams& p, int t) {
   PTile r;
   r.nt = t % p.ntiles;
   const int rest = t / p.ntiles;
-  r.mt = 2 * (rest % p.mpairs) + static_cast<int>(rank);
-  r.b = rest / p.mpairs;
+  r.mt = rest % p.mtiles;
+  r.b = rest / p.mtiles;
   return r;
 }
 
 template <int BN>
-__device__ void p_producer(const ProdParams& p, const PShared& s, int total, uint32_t rank,
-                           int cl, int ncl) {
+__device__ void p_producer(const ProdParams& p, const PShared& s, int total, int cl, int ncl) {
   constexpr uint32_t kStage = kPABytes + BN * kProdTileK * 2;
-  constexpr uint32_t kHalfB = BN / 2 * kProdTileK * 2;
   const int ksteps = p.c / kProdTileK;
   // W is re-read for every token tile: keep it in L2 ahead of the streams
   const uint64_t keep = policy_evict_last();
@@ -129,18 +124,16 @@ __device__ void p_producer(const ProdParams& p, const PShared& s, int total, uin
     }
   };
   for (int t = cl; t < total; t += ncl) {
-    const PTile tl = decode(p, t, rank);
+    const PTile tl = decode(p, t);
     for (int kt = 0; kt < ksteps; ++kt) {
-      // both CTAs' MMAs have released the slot: the peer's half may land too
       if (!pwait(s, pbar(s, PB_EMPTY0 + slot), phase ^ 1u, kStatusTimeoutProducer))
         return drain();
       const uint32_t dst = s.stages + slot * kStage;
-      mbar_arrive_expect_tx(pbar(s, PB_FULL0 + slot), kStage);  // own x, both W halves
+      mbar_arrive_expect_tx(pbar(s, PB_FULL0 + slot), kStage);
       tma_load_3d(dst, &p.tm_x, pbar(s, PB_FULL0 + slot), kt * kProdTileK, tl.mt * kProdTileM,
                   tl.b);
-      tma_load_2d_mc_hint(dst + kPABytes + rank * kHalfB, &p.tm_w, pbar(s, PB_FULL0 + slot),
-                          kt * kProdTileK, tl.nt * BN + static_cast<int>(rank) * (BN / 2), 0x3,
-                          keep);
+      tma_load_2d_hint(dst + kPABytes, &p.tm_w, pbar(s, PB_FULL0 + slot), kt * kProdTileK,
+                       tl.nt * BN, keep);
       last_phase = (last_phase & ~(1u << slot)) | (phase << slot);
       issued |= 1u << slot;
       if (++slot == kPStages) {
@@ -173,7 +166,7 @@ __device__ void p_mma(const ProdParams& p, const PShared& s, int total, uint32_t
 #pragma unroll
       for (int kk = 0; kk < kProdTileK / 16; ++kk)
         mma_ss(d, ad + 2 * kk, bd + 2 * kk, idesc, (kt | kk) != 0 ? 1u : 0u);
-      tc_commit_mc(pbar(s, PB_EMPTY0 + slot), 0x3);  // release the slot in both CTAs
+      tc_commit(pbar(s, PB_EMPTY0 + slot));  // the slot may be refilled
       if (++slot == kPStages) {
         slot = 0;
         phase ^= 1u;
@@ -228,7 +221,7 @@ __device__ __forceinline__ uint32_t bf16x2(float lo, float hi) {
 
 template <int D, int BN>
 __device__ void p_epilogue(const ProdParams& p, const PShared& s, int total, uint32_t tbase,
-                           uint32_t rank, int cl, int ncl) {
+                           int cl, int ncl) {
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
   const int wq = warp - kPEpiWarp0;  // TMEM lanes 32 wq .. 32 wq + 31
   const int r = 32 * wq + lane;
@@ -238,7 +231,7 @@ __device__ void p_epilogue(const ProdParams& p, const PShared& s, int total, uin
   griddep_wait();  // 1/rms comes from the pre-pass, which may still be running
   uint32_t it = 0, ob = 0;
   for (int t = cl; t < total; t += ncl, ++it) {
-    const PTile tl = decode(p, t, rank);
+    const PTile tl = decode(p, t);
     const uint32_t ab = it & 1u, use = it >> 1;
     const bool ok = pwait(s, pbar(s, PB_ACCFULL0 + ab), use & 1u, kStatusTimeoutSoftmax);
     if (!__all_sync(0xffffffffu, ok)) return;
@@ -285,7 +278,7 @@ __device__ void p_epilogue(const ProdParams& p, const PShared& s, int total, uin
       uint32_t pk[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) pk[i] = bf16x2(y[2 * i], y[2 * i + 1]);
-      if (kind == 1 && tl.mt < p.mtiles) {
+      if (kind == 1) {
         // sums of the stored (rounded) keys; rows past N hold zeros
         float a[64];
 #pragma unroll
@@ -334,14 +327,13 @@ __global__ void __launch_bounds__(kPThreads, 1) produce_kernel(const __grid_cons
   s.abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   s.status = p.status;
   const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-  const int total = p.batch * p.mpairs * p.ntiles;  // work units of a cluster
-  const uint32_t rank = cluster_ctarank();
-  const int cl = static_cast<int>(blockIdx.x / 2), ncl = static_cast<int>(gridDim.x / 2);
+  const int total = p.batch * p.mtiles * p.ntiles;  // work units
+  const int cl = static_cast<int>(blockIdx.x), ncl = static_cast<int>(gridDim.x);
 
   if (threadIdx.x == 0) {
     for (int i = 0; i < kPStages; ++i) {
       mbar_init(pbar(s, PB_FULL0 + i), 1);
-      mbar_init(pbar(s, PB_EMPTY0 + i), 2);  // both CTAs' MMAs release a slot
+      mbar_init(pbar(s, PB_EMPTY0 + i), 1);
     }
     for (int i = 0; i < 2; ++i) {
       mbar_init(pbar(s, PB_ACCFULL0 + i), 1);
@@ -361,22 +353,20 @@ __global__ void __launch_bounds__(kPThreads, 1) produce_kernel(const __grid_cons
   }
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // the peer's barriers are initialised before any multicast reaches them
   tc_fence_after();
   const uint32_t tbase = *tslot;
 
   if (warp == 0) {
-    if (lane == 0) p_producer<BN>(p, s, total, rank, cl, ncl);
+    if (lane == 0) p_producer<BN>(p, s, total, cl, ncl);
   } else if (warp == 1) {
     if (lane == 0) p_mma<BN>(p, s, total, tbase, cl, ncl);
   } else if (warp >= kPEpiWarp0) {
-    p_epilogue<D, BN>(p, s, total, tbase, rank, cl, ncl);
+    p_epilogue<D, BN>(p, s, total, tbase, cl, ncl);
     if (lane == 0) bulk_wait_all();  // the tile stores must be complete before the CTA exits
   }
 
   tc_fence_before();
   __syncthreads();
-  cluster_sync();  // no CTA leaves while its peer may still signal its barriers
   tc_fence_after();
   if (warp == 2) tmem_dealloc(tbase, 2 * BN);
 }
@@ -447,49 +437,25 @@ __global__ void __launch_bounds__(32 * kRedRows) reduce_key_sums(const float* __
   }
 }
 
-// Clusters of two CTAs, as many as can be resident at once (a persistent
-// grid: clusters beyond that would wait for a second wave).
+// A persistent grid: one CTA per SM, at most one per work unit.
 template <int D, int BN>
 cudaError_t launch_gemm(const ProdParams& p, int max_ctas, cudaStream_t stream) {
-  static int max_clusters_of[kMaxDevices] = {};  // 0: not configured yet
+  static bool attr_set[kMaxDevices] = {};
   const int dev = current_device();
   if (dev < 0) return cudaErrorInvalidDevice;
-  int& max_clusters = max_clusters_of[dev];
   const size_t smem = produce_smem_bytes(BN);
-  cudaLaunchConfig_t cfg = {};
-  cudaLaunchAttribute attr[2];
-  attr[0].id = cudaLaunchAttributeClusterDimension;
-  attr[0].val.clusterDim.x = 2;
-  attr[0].val.clusterDim.y = 1;
-  attr[0].val.clusterDim.z = 1;
+  if (!attr_set[dev]) {
+    const cudaError_t e = cudaFuncSetAttribute(
+        produce_kernel<D, BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
+    if (e != cudaSuccess) return e;
+    attr_set[dev] = true;
+  }
+  const int units = p.batch * p.mtiles * p.ntiles;
+  int grid = max_ctas < units ? max_ctas : units;
+  if (grid < 1) grid = 1;
   // dependent launch: the GEMM's main loop (x and W only) overlaps the RMS
   // pre-pass; the epilogue waits for its 1/rms values
-  attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
-  attr[1].val.programmaticStreamSerializationAllowed = 1;
-  cfg.blockDim = dim3(kPThreads);
-  cfg.dynamicSmemBytes = smem;
-  cfg.stream = stream;
-  cfg.attrs = attr;
-  cfg.numAttrs = 1;  // the occupancy query takes the cluster shape alone
-  if (max_clusters == 0) {
-    cudaError_t e = cudaFuncSetAttribute(produce_kernel<D, BN>,
-                                         cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         static_cast<int>(smem));
-    if (e != cudaSuccess) return e;
-    cfg.gridDim = dim3(2);
-    int n = 0;
-    e = cudaOccupancyMaxActiveClusters(&n, produce_kernel<D, BN>, &cfg);
-    if (e != cudaSuccess) return e;
-    if (n < 1) return cudaErrorInvalidConfiguration;
-    max_clusters = n;
-  }
-  const int units = p.batch * p.mpairs * p.ntiles;
-  int clusters = max_ctas / 2 < max_clusters ? max_ctas / 2 : max_clusters;
-  if (clusters > units) clusters = units;
-  if (clusters < 1) clusters = 1;
-  cfg.gridDim = dim3(2 * clusters);
-  cfg.numAttrs = 2;
-  return cudaLaunchKernelEx(&cfg, produce_kernel<D, BN>, p);
+  return launch_dependent(produce_kernel<D, BN>, dim3(grid), dim3(kPThreads), smem, stream, p);
 }
 
 }  // namespace

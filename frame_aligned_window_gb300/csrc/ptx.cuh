@@ -60,17 +60,6 @@ __device__ __forceinline__ void tma_load_2d(uint32_t dst, const CUtensorMap* map
       : "memory");
 }
 
-// 2-D tiled load written to the same shared-memory offset in every CTA of
-// the cluster named in cta_mask; each destination CTA's mbarrier at `bar`'s
-// offset receives the transaction bytes.
-__device__ __forceinline__ void tma_load_2d_mc(uint32_t dst, const CUtensorMap* map, uint32_t bar,
-                                               int32_t x, int32_t y, uint16_t cta_mask) {
-  asm volatile(
-      "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask)
-      : "memory");
-}
 // L2 eviction-priority policies for the .L2::cache_hint forms below.
 __device__ __forceinline__ uint64_t policy_evict_last() {
   uint64_t p;
@@ -90,14 +79,13 @@ __device__ __forceinline__ uint4 ld_stream_v4(const uint4* p, uint64_t policy) {
                : "l"(p), "l"(policy));
   return v;
 }
-// tma_load_2d_mc with an L2 eviction policy for the loaded lines.
-__device__ __forceinline__ void tma_load_2d_mc_hint(uint32_t dst, const CUtensorMap* map,
-                                                    uint32_t bar, int32_t x, int32_t y,
-                                                    uint16_t cta_mask, uint64_t policy) {
+// tma_load_2d with an L2 eviction policy for the loaded lines.
+__device__ __forceinline__ void tma_load_2d_hint(uint32_t dst, const CUtensorMap* map, uint32_t bar,
+                                                 int32_t x, int32_t y, uint64_t policy) {
   asm volatile(
       "cp.async.bulk.tensor.2d.shared::cluster.global.mbarrier::complete_tx::bytes"
-      ".multicast::cluster.L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5, %6;" ::"r"(dst),
-      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "h"(cta_mask), "l"(policy)
+      ".L2::cache_hint [%0], [%1, {%3, %4}], [%2], %5;" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(bar), "r"(x), "r"(y), "l"(policy)
       : "memory");
 }
 // tma_store_3d with an L2 eviction policy for the written lines.
@@ -171,18 +159,6 @@ __device__ __forceinline__ void griddep_launch_dependents() {
   asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
 }
 
-// ------------------------------------------------------------------ cluster
-__device__ __forceinline__ uint32_t cluster_ctarank() {
-  uint32_t r;
-  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
-  return r;
-}
-// Every thread of every CTA of the cluster arrives, then waits for all (the
-// non-.aligned form: the warp need not be converged).
-__device__ __forceinline__ void cluster_sync() {
-  asm volatile("barrier.cluster.arrive.release;\n\tbarrier.cluster.wait.acquire;" ::: "memory");
-}
-
 // ------------------------------------------------------------------- tcgen05
 __device__ __forceinline__ void tmem_alloc(uint32_t dst_smem, uint32_t ncols) {
   asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(dst_smem),
@@ -207,15 +183,6 @@ __device__ __forceinline__ void tc_fence_after() {
 __device__ __forceinline__ void tc_commit(uint32_t bar) {
   asm volatile(
       "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
-      : "memory");
-}
-// Like tc_commit, arriving on the mbarrier at `bar`'s offset in every CTA of
-// the cluster named in cta_mask.
-__device__ __forceinline__ void tc_commit_mc(uint32_t bar, uint16_t cta_mask) {
-  asm volatile(
-      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.multicast::cluster.b64"
-      " [%0], %1;" ::"r"(bar),
-      "h"(cta_mask)
       : "memory");
 }
 // D[tmem] = A * B (+ D if accum): A and B both described in shared memory.

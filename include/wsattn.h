@@ -194,9 +194,11 @@ int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, 
  * exists for callers that must not let the library allocate device memory
  * (a host framework that owns all device memory through its own pool or a
  * fixed budget, or a latency-critical loop that cannot take cudaMalloc's
- * implicit synchronisation).  It computes the same statistics as
- * wsattn_prepare, with no plan, into buffers the caller owns, and never
- * calls cudaMalloc, cudaFree or any other allocating routine.
+ * implicit synchronisation).  It computes, with no plan, into buffers the
+ * caller owns, the statistics wsattn_prepare computes on a plan left at the
+ * default global bound (WSATTN_BOUND_GLOBAL): window bounds and mask flags
+ * do not apply.  It never calls cudaMalloc, cudaFree or any other
+ * allocating routine.
  *   batch, heads, n_tokens, head_dim   shape of q and k ([batch, heads,
  *                     n_tokens, head_dim] bf16, 16-byte aligned); head_dim
  *                     64 or 128
@@ -208,7 +210,8 @@ int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, 
  * Its scratch is one fixed array in the library's device image: 2048 chunk
  * slots (1,064,960 bytes), held by every GPU that loads the library until
  * the process exits.  batch*heads above 2048 is rejected with BAD_ARG before
- * anything is enqueued.  All calls share the array and it keeps the last
+ * anything is enqueued (so is a row chunking that would need more than the
+ * 2048 slots, which cannot happen on a GPU with fewer than 683 SMs).  All calls share the array and it keeps the last
  * call's contents; nothing in it needs to start at zero.  Calls whose
  * kernels can overlap on the GPU race on it and must be ordered by the
  * caller.  The first call on a device looks up the array's device address
@@ -278,7 +281,9 @@ int wsattn_plan_set_bound(wsattn_plan_t plan, int mode);
 
 /* Synchronises `stream` and reports the plan's device status word: OK, or
  * TIMEOUT if a device-side wait of a kernel launched with this plan expired
- * (the word is then cleared).  CUDA if the synchronisation itself failed. */
+ * (the word is then cleared, and so are the plan's forward work counters,
+ * which a forward that gave up may have left mid-count).  CUDA if the
+ * synchronisation itself failed. */
 int wsattn_device_status(wsattn_plan_t plan, void* stream);
 
 /* Failure-path self test: launches a one-thread kernel that waits on a

@@ -84,3 +84,37 @@ def test_tau_override_changes_eligibility():
     want = oracle_prepare_all(wl, q, k, tau=10.0)
     np.testing.assert_array_equal(st["elig"], want["elig"])
     assert not st["elig"].any()
+
+
+def test_underflow_clause_decides_eligibility_and_forward_matches():
+    # Google Developers Blog post "HeyGen x Google Cloud: Bringing Avatar IV
+    # to TPUs", section "Breaking softmax's dependency chain": with a loose
+    # bound the fixed-max exponentials underflow.  With tau raised to 50, a
+    # head whose B_h lies in (63 ln 2, 50] = (43.67, 50] passes the tau test
+    # but fails the row clause 2 b_i < 126 ln 2, so it must run the online
+    # path.  Head 3 of 'small' gets its queries scaled so that B_h is about 46;
+    # the other heads stay near 17.
+    import frame_aligned_window_gb300 as fw
+    from _helpers import gpu_run, oracle_rows, rel_l2, TOL_MAX_ABS, TOL_REL_L2
+    wl = workload("small")
+    q, k, v = generate(wl)
+    base = oracle_prepare_all(wl, q, k)
+    head = 3
+    q = q.clone()
+    q[0, head] = (q[0, head].double() * (46.0 / base["bmax"][head])).to(torch.bfloat16)
+    tau = 50.0
+    want = oracle_prepare_all(wl, q, k, tau=tau)
+    limit = 63.0 * np.log(2.0)
+    assert limit * 1.001 < want["bmax"][head] < tau / 1.001
+    assert (np.delete(want["bmax"], head) < limit / 1.001).all()
+    assert want["elig"][head] == 0 and np.delete(want["elig"], head).all()
+    plan, out, _ = gpu_run(wl, q, k, v, tau=tau)
+    st = fw.wsattn_get_stats(plan, wl.batch)
+    np.testing.assert_array_equal(st["elig"], want["elig"])
+    np.testing.assert_allclose(st["bmax"], want["bmax"], rtol=REL_BOUND)
+    # the ineligible head's output (every row) against the oracle
+    rows = list(range(wl.n_tokens))
+    ref = oracle_rows(wl, q, k, v, [(0, head)], rows)[0]
+    got = flat_heads(out.cpu(), wl)[head].double().numpy()
+    err = float(np.abs(got - ref).max())
+    assert err <= TOL_MAX_ABS and rel_l2(got, ref) <= TOL_REL_L2, err

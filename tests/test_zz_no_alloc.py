@@ -3,12 +3,14 @@ the library allocate device memory (a framework that owns all device memory
 through its own pool or budget, or a latency-critical loop that cannot take
 cudaMalloc's implicit synchronisation).
 
-The entry point is called through the C ABI on two calls in a row, with
-different shapes, and each result is checked against the statistics the
-allocating entry point (wsattn_prepare) computes for the same input, within
-the tolerances the prepare parity tests use.  The output buffers are filled
-with NaN first, so every value checked was written by the call.  Free device
-memory is unchanged across the second call.
+The entry point is called through the C ABI three times in a row: two
+different shapes, then the second shape again.  Each result is checked
+against the statistics the allocating entry point (wsattn_prepare) computes
+for the same input, and against the fp64 oracle directly, within the
+tolerances the prepare parity tests use.  The output buffers are filled with
+NaN first, so every value checked was written by the call.  Free device
+memory is unchanged across the third call, which follows a call of the same
+shape (so nothing is looked up or created on its behalf).
 """
 import ctypes
 
@@ -16,6 +18,8 @@ import numpy as np
 import pytest
 import torch
 
+import oracle
+from _helpers import flat_heads, oracle_prepare_all
 from workloads import WORKLOADS, generate
 
 pytestmark = pytest.mark.gpu
@@ -52,9 +56,24 @@ def _check_against(out, ref):
         np.testing.assert_allclose(got[key], ref[key], rtol=REL, atol=1e-6)
 
 
-def test_prepare_static_two_calls_match_prepare():
+def _check_against_oracle(wl, q, k, out):
+    got = {key: t.cpu().numpy().reshape(wl.batch * wl.heads, -1) for key, t in out.items()}
+    want = oracle_prepare_all(wl, q, k)
+    assert (np.abs(want["bmax"] - oracle.TAU) / oracle.TAU > 1e-3).all()
+    np.testing.assert_array_equal(got["elig"].ravel(), want["elig"])
+    np.testing.assert_allclose(got["mu"], want["mu"], rtol=0, atol=2e-5)
+    np.testing.assert_allclose(got["kmax"].ravel(), want["kmax"], rtol=REL)
+    np.testing.assert_allclose(got["bmax"].ravel(), want["bmax"], rtol=REL)
+    np.testing.assert_allclose(got["b"], want["b"], rtol=REL, atol=1e-6)
+    qf = flat_heads(q, wl).double().numpy()
+    m_want = want["b"] + wl.scale * np.einsum("hnd,hd->hn", qf, want["mu"])
+    np.testing.assert_allclose(got["m"], m_want, rtol=0,
+                               atol=1e-5 * (1 + np.abs(m_want).max()))
+
+
+def test_prepare_static_calls_in_a_row_match_prepare_and_oracle():
     import frame_aligned_window_gb300 as fw
-    for call, name in enumerate(["small", "tiny"]):
+    for call, name in enumerate(["small", "tiny", "tiny"]):
         wl = WORKLOADS[name]
         q, k, v = generate(wl)
         qd, kd = q.cuda(), k.cuda()
@@ -66,9 +85,10 @@ def test_prepare_static_two_calls_match_prepare():
         free_before = torch.cuda.mem_get_info()[0]
         assert _call_static(wl, qd, kd, out) == 0
         torch.cuda.synchronize()
-        if call == 1:
+        if call == 2:
             assert torch.cuda.mem_get_info()[0] == free_before
         _check_against(out, ref)
+        _check_against_oracle(wl, q, k, out)
         assert torch.equal(kd.cpu(), k) and torch.equal(qd.cpu(), q)
 
 
