@@ -14,12 +14,13 @@
 //   - "Proving pixels unchanged": the PV product takes P in bf16.
 //
 // Persistent kernel, one CTA per SM, 12 warps:
-//   warp 0      TMA producer: Q tile (128 x D) into a staging buffer; K and V
-//               steps into two rings, all 128-byte swizzled.
+//   warps 0, 2  TMA producers (one thread each): warp 0 loads the Q tile
+//               (128 x D) into a staging buffer and the K steps, warp 2 the V
+//               steps, into two rings, all 128-byte swizzled.
 //   warps 1, 3  MMA issuers (one thread each): S = Q K^T and O += P V with
 //               tcgen05.mma kind::f16 (bf16 in, fp32 accumulate in TMEM).
 //               Q and P are read from TMEM, K and V from shared memory.
-//   warp 2      allocates and frees tensor memory.
+//               Warp 2 also allocates and frees tensor memory.
 //   warps 4-11  two softmax + epilogue warpgroups (kNumWG).  Thread i of a
 //               warpgroup owns row i of the tile (TMEM lane i); the 16-column
 //               chunks of a key step are split over the warpgroups in order
@@ -78,7 +79,7 @@ constexpr uint32_t kTmemCols = 512;
 // from a global counter and passes it to the CTA's other roles through a
 // small queue in shared memory.
 constexpr int kItemQueue = 4;
-constexpr uint32_t kItemReaders = 2 + kSoftmaxWarps;  // both issuers and every softmax warp
+constexpr uint32_t kItemReaders = 3 + kSoftmaxWarps;  // V producer, both issuers, every softmax warp
 
 // mbarrier slots
 enum : int {
@@ -306,21 +307,24 @@ __device__ __noinline__ void drain_loads(uint32_t full0, int n, uint32_t phase, 
   }
 }
 
+// Two producer threads: one loads each tile's Q and its K steps, the other
+// its V steps.  With one thread issuing in consumption order (K0, K1, V0, K2,
+// V1, ...), a K load waited behind the V load before it, whose slot frees
+// later (PV runs behind QK), and K arrived with half its lead.
 template <int D>
-__device__ void producer(const FwdParams& p, const Shared& s) {
+__device__ void producer_qk(const FwdParams& p, const Shared& s) {
   constexpr int kBoxes = D / 64;
   const int bk = p.bk, G = p.G;
   const uint32_t ns = static_cast<uint32_t>(G * bk);     // rows of a step
   const uint32_t box_pitch = ns * 128u;                  // a 64-column box of a stage
   const uint32_t stage_bytes = box_pitch * kBoxes;
-  const uint32_t nk = static_cast<uint32_t>(p.stages_k), nv = static_cast<uint32_t>(p.stages_v);
-  Ring kr, vr;
+  const uint32_t nk = static_cast<uint32_t>(p.stages_k);
+  Ring kr;
   uint32_t qc = 0;
-  // parity of the last load issued into each K / V slot (for drain_loads)
-  uint32_t kph = 0, vph = 0, kiss = 0, viss = 0;
+  // parity of the last load issued into each K slot (for drain_loads)
+  uint32_t kph = 0, kiss = 0;
   auto drain = [&]() {
     drain_loads(bar(s, B_KFULL0), static_cast<int>(nk), kph, kiss);
-    drain_loads(bar(s, B_VFULL0), static_cast<int>(nv), vph, viss);
     drain_loads(bar(s, B_QFULL), 1, (qc - 1u) & 1u, qc > 0 ? 1u : 0u);
   };
   const int n_items = p.n_tiles * p.bh;
@@ -338,39 +342,59 @@ __device__ void producer(const FwdParams& p, const Shared& s) {
     for (int c = 0; c < kBoxes; ++c)
       tma_load_2d(s.q + c * (kTileM * 128), &p.tm_q, bar(s, B_QFULL), c * 64, y0 + t.row0);
     ++qc;
-    Steps ks, vs;
+    Steps ks;
     ks.init(t);
+    for (int j = 0; j < t.nstep; ++j) {
+      int nb;
+      const int row = y0 + ks.next(G, nb) * bk;
+      if (!wait(s, bar(s, B_KEMPTY0 + kr.slot), kr.phase ^ 1u, kStatusTimeoutProducer))
+        return drain();
+      const uint32_t fb = bar(s, B_KFULL0 + kr.slot);
+      mbar_arrive_expect_tx(fb, stage_bytes);
+      const uint32_t dst = s.k + kr.slot * stage_bytes;
+#pragma unroll
+      for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_k, fb, c * 64, row);
+      kph = (kph & ~(1u << kr.slot)) | (kr.phase << kr.slot);
+      kiss |= 1u << kr.slot;
+      kr.next(nk);
+    }
+  }
+}
+
+template <int D>
+__device__ void producer_v(const FwdParams& p, const Shared& s) {
+  constexpr int kBoxes = D / 64;
+  const int bk = p.bk, G = p.G;
+  const uint32_t ns = static_cast<uint32_t>(G * bk);
+  const uint32_t box_pitch = ns * 128u;
+  const uint32_t stage_bytes = box_pitch * kBoxes;
+  const uint32_t nv = static_cast<uint32_t>(p.stages_v);
+  Ring vr;
+  uint32_t vph = 0, viss = 0;
+  auto drain = [&]() { drain_loads(bar(s, B_VFULL0), static_cast<int>(nv), vph, viss); };
+  ItemPos iq;
+  while (true) {
+    const int it = read_item(s, iq, kStatusTimeoutProducer);
+    if (it == -2) return drain();
+    if (it < 0) break;
+    const Item im = map_item(p, it);
+    const WorkTile t = p.tiles[im.tile];
+    const int y0 = im.bh * p.n;
+    Steps vs;
     vs.init(t);
-    // Issue order follows consumption: K0, K1, V0, K2, V1, ...
-    for (int j = 0; j <= t.nstep; ++j) {
-      if (j < t.nstep) {
-        int nb;
-        const int row = y0 + ks.next(G, nb) * bk;
-        if (!wait(s, bar(s, B_KEMPTY0 + kr.slot), kr.phase ^ 1u, kStatusTimeoutProducer))
-          return drain();
-        const uint32_t fb = bar(s, B_KFULL0 + kr.slot);
-        mbar_arrive_expect_tx(fb, stage_bytes);
-        const uint32_t dst = s.k + kr.slot * stage_bytes;
+    for (int j = 0; j < t.nstep; ++j) {
+      int nb;
+      const int row = y0 + vs.next(G, nb) * bk;
+      if (!wait(s, bar(s, B_VEMPTY0 + vr.slot), vr.phase ^ 1u, kStatusTimeoutProducer))
+        return drain();
+      const uint32_t fb = bar(s, B_VFULL0 + vr.slot);
+      mbar_arrive_expect_tx(fb, stage_bytes);
+      const uint32_t dst = s.v + vr.slot * stage_bytes;
 #pragma unroll
-        for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_k, fb, c * 64, row);
-        kph = (kph & ~(1u << kr.slot)) | (kr.phase << kr.slot);
-        kiss |= 1u << kr.slot;
-        kr.next(nk);
-      }
-      if (j >= 1) {
-        int nb;
-        const int row = y0 + vs.next(G, nb) * bk;
-        if (!wait(s, bar(s, B_VEMPTY0 + vr.slot), vr.phase ^ 1u, kStatusTimeoutProducer))
-          return drain();
-        const uint32_t fb = bar(s, B_VFULL0 + vr.slot);
-        mbar_arrive_expect_tx(fb, stage_bytes);
-        const uint32_t dst = s.v + vr.slot * stage_bytes;
-#pragma unroll
-        for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_v, fb, c * 64, row);
-        vph = (vph & ~(1u << vr.slot)) | (vr.phase << vr.slot);
-        viss |= 1u << vr.slot;
-        vr.next(nv);
-      }
+      for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_v, fb, c * 64, row);
+      vph = (vph & ~(1u << vr.slot)) | (vr.phase << vr.slot);
+      viss |= 1u << vr.slot;
+      vr.next(nv);
     }
   }
 }
@@ -839,7 +863,9 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
   griddep_wait();  // the row maxima and eligibility come from the kernel before
 
   if (warp == 0) {
-    if (lane == 0) producer<D>(p, s);
+    if (lane == 0) producer_qk<D>(p, s);
+  } else if (warp == 2) {
+    if (lane == 0) producer_v<D>(p, s);
   } else if (warp == 1) {
     if (lane == 0) qk_issuer<D>(p, s, tbase);
   } else if (warp == 3) {
