@@ -17,7 +17,8 @@
 //   warps 0, 2  TMA producers (one thread each): warp 0 loads the Q tile
 //               (128 x D) into a staging buffer and the K steps, warp 2 the V
 //               steps, into two rings, all 128-byte swizzled.
-//   warps 1, 3  MMA issuers (one thread each): S = Q K^T and O += P V with
+//   warps 1, 3  MMA issuers (whole warps, one elected lane issuing each
+//               instruction): S = Q K^T and O += P V with
 //               tcgen05.mma kind::f16 (bf16 in, fp32 accumulate in TMEM).
 //               Q and P are read from TMEM, K and V from shared memory.
 //               Warp 2 also allocates and frees tensor memory.
@@ -191,6 +192,22 @@ __device__ __forceinline__ int read_item(const Shared& s, ItemPos& q, int code) 
   if (!wait(s, bar(s, B_IQFULL0 + q.slot), q.phase, code)) return -2;
   const int it = s.iq[q.slot];
   mbar_arrive(bar(s, B_IQEMPTY0 + q.slot));
+  q.next();
+  return it;
+}
+
+// The MMA issuers are whole warps (each instruction issued by one elected
+// lane): every lane waits, and the warp reconverges before the next MMA.
+__device__ __forceinline__ bool wait_issuer(const Shared& s, uint32_t b, uint32_t parity) {
+  return __all_sync(0xffffffffu, wait(s, b, parity, kStatusTimeoutMma));
+}
+
+// An issuer warp's next work item: every lane waits and reads, one arrives.
+__device__ __forceinline__ int read_item_issuer(const Shared& s, ItemPos& q) {
+  if (!wait_issuer(s, bar(s, B_IQFULL0 + q.slot), q.phase)) return -2;
+  const int it = s.iq[q.slot];
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar(s, B_IQEMPTY0 + q.slot));
   q.next();
   return it;
 }
@@ -400,12 +417,13 @@ __device__ void producer_v(const FwdParams& p, const Shared& s) {
 }
 
 // ---------------------------------------------------------------- MMA issue
-// Two single-thread issuers feed the tensor core: warp 1 issues S = Q K^T,
-// warp 3 issues O += P V.  A tcgen05.mma blocks its issuing thread while the
-// MMA queue is full, so with one issuer every barrier wait and every bit of
-// bookkeeping between MMA groups left the tensor core idle; with two, one
-// issuer's waits overlap the other's MMAs.  QK^T(j+1) waits only until every
-// softmax warp holds S(j) in registers; PV(j) waits for P(j).
+// Two issuer warps feed the tensor core: warp 1 issues S = Q K^T, warp 3
+// issues O += P V, each instruction from one elected lane of the converged
+// warp.  A tcgen05.mma blocks its issuing thread while the MMA queue is
+// full, so with one issuer every barrier wait and every bit of bookkeeping
+// between MMA groups left the tensor core idle; with two, one issuer's waits
+// overlap the other's MMAs.  QK^T(j+1) waits only until every softmax warp
+// holds S(j) in registers; PV(j) waits for P(j).
 // Descriptor bases are computed once; each MMA adds a constant to the
 // start-address field (bits 0-13, address >> 4), and the k-step loops are
 // unrolled.
@@ -429,12 +447,12 @@ __device__ void qk_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
   Steps qs;
   ItemPos iq;
   while (true) {
-    const int it = read_item(s, iq, kStatusTimeoutMma);
+    const int it = read_item_issuer(s, iq);
     if (it < 0) break;
     const Item im = map_item(p, it);
     const WorkTile t = p.tiles[im.tile];
     qs.init(t);
-    if (!wait(s, bar(s, B_QTFULL), tiles_done & 1u, kStatusTimeoutMma)) return;
+    if (!wait_issuer(s, bar(s, B_QTFULL), tiles_done & 1u)) return;
     tc_fence_after();
     for (int j = 0; j < t.nstep; ++j) {
       int nb;
@@ -443,17 +461,17 @@ __device__ void qk_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
       const uint32_t slot = kr.slot;
       // K is normally resident long before S is free: wait for it first, so
       // the wait that gates the MMAs is the softmax's.
-      if (!wait(s, bar(s, B_KFULL0 + slot), kr.phase, kStatusTimeoutMma)) return;
+      if (!wait_issuer(s, bar(s, B_KFULL0 + slot), kr.phase)) return;
       // the softmax warps must hold the previous S in registers
-      if (!wait(s, bar(s, B_SEMPTY), su ^ 1u, kStatusTimeoutMma)) return;
+      if (!wait_issuer(s, bar(s, B_SEMPTY), su ^ 1u)) return;
       tc_fence_after();
       const uint64_t kd = kdesc0 + slot * stage16;
       const uint32_t id = id_qk0 | ((keys >> 3) << 17);
 #pragma unroll
       for (int kk = 0; kk < D / 16; ++kk)
-        mma_ts(t_s, t_q + kk * 8, kd + (kk / 4) * box16 + (kk % 4) * 2, id, kk > 0 ? 1u : 0u);
-      tc_commit(bar(s, B_KEMPTY0 + slot));
-      tc_commit(bar(s, B_SFULL));
+        mma_ts_warp(t_s, t_q + kk * 8, kd + (kk / 4) * box16 + (kk % 4) * 2, id, kk > 0 ? 1u : 0u);
+      tc_commit_warp(bar(s, B_KEMPTY0 + slot));
+      tc_commit_warp(bar(s, B_SFULL));
       kr.next(nk);
       su ^= 1u;
     }
@@ -479,7 +497,7 @@ __device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
   Steps ps;
   ItemPos iq;
   while (true) {
-    const int it = read_item(s, iq, kStatusTimeoutMma);
+    const int it = read_item_issuer(s, iq);
     if (it < 0) break;
     const Item im = map_item(p, it);
     const WorkTile t = p.tiles[im.tile];
@@ -491,23 +509,23 @@ __device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
       const int keys = nb * bk;
       const int nks = keys / 16;
       const uint32_t pb = pr.slot;
-      if (!wait(s, bar(s, B_PFULL0 + pb), pr.phase, kStatusTimeoutMma)) return;
+      if (!wait_issuer(s, bar(s, B_PFULL0 + pb), pr.phase)) return;
       const uint32_t vslot = vr.slot;
-      if (!wait(s, bar(s, B_VFULL0 + vslot), vr.phase, kStatusTimeoutMma)) return;
+      if (!wait_issuer(s, bar(s, B_VFULL0 + vslot), vr.phase)) return;
       tc_fence_after();
       const uint64_t vd = vdesc0 + vslot * stage16;
       const uint32_t a_p = t_p + pb * tc_.pstride;
       // 16 key rows (2 KB of V, 8 P columns) per k-step
-      mma_ts(t_o, a_p, vd, id_pv, j > 0 ? 1u : 0u);
+      mma_ts_warp(t_o, a_p, vd, id_pv, j > 0 ? 1u : 0u);
 #pragma unroll
       for (int kk = 1; kk < kNumWG * MAXC; ++kk)
-        if (kk < nks) mma_ts(t_o, a_p + kk * 8, vd + kk * 128, id_pv, 1u);
-      tc_commit(bar(s, B_VEMPTY0 + vslot));
-      tc_commit(bar(s, B_PVDONE0 + pb));
+        if (kk < nks) mma_ts_warp(t_o, a_p + kk * 8, vd + kk * 128, id_pv, 1u);
+      tc_commit_warp(bar(s, B_VEMPTY0 + vslot));
+      tc_commit_warp(bar(s, B_PVDONE0 + pb));
       vr.next(nv);
       pr.next(2);
     }
-    tc_commit(bar(s, B_OFULL));
+    tc_commit_warp(bar(s, B_OFULL));
   }
 }
 
@@ -867,9 +885,9 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
   } else if (warp == 2) {
     if (lane == 0) producer_v<D>(p, s);
   } else if (warp == 1) {
-    if (lane == 0) qk_issuer<D>(p, s, tbase);
+    qk_issuer<D>(p, s, tbase);
   } else if (warp == 3) {
-    if (lane == 0) pv_issuer<D, MAXC>(p, s, tbase);
+    pv_issuer<D, MAXC>(p, s, tbase);
   } else if (warp >= kSoftmaxWarp0) {
     softmax_wg<D, MAXC>(p, s, tbase);
     // the epilogue's tile stores must be complete before the CTA exits
