@@ -108,6 +108,18 @@ class ClockSampler:
             except subprocess.TimeoutExpired:
                 self.proc.kill()
 
+    def samples_between(self, t0, t1):
+        """SM MHz of the samples taken between host times t0 and t1."""
+        out = []
+        for t, line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) >= 2 and t0 <= t <= t1:
+                try:
+                    out.append(float(parts[1]))
+                except ValueError:
+                    pass
+        return out
+
     def summary(self):
         if self.proc is None:
             return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
@@ -311,6 +323,7 @@ def run_gpu(args, wl, world, rank, local):
     torch.cuda.synchronize()
     if clocks:
         clocks.mark_start()
+    host_t0 = time.time()
     t_begin = torch.cuda.Event(enable_timing=True)
     t_end = torch.cuda.Event(enable_timing=True)
     t_begin.record(stream)
@@ -332,6 +345,23 @@ def run_gpu(args, wl, world, rank, local):
     total_ms = t_begin.elapsed_time(t_end)
     prep_ms = [e0.elapsed_time(e1) for e0, e1, _ in ev]
     fwd_ms = [e1.elapsed_time(e2) for _, e1, e2 in ev]
+    # The timed steps in (up to) five consecutive bins: forward ms per bin and
+    # the SM clock samples that fall inside it (GPU time mapped to host time
+    # from the synchronised start), so a drift in time per step can be told
+    # apart from a drift in clock.
+    bins = []
+    nb = min(5, args.steps)
+    for i in range(nb):
+        a, b = i * args.steps // nb, (i + 1) * args.steps // nb
+        if b <= a:
+            continue
+        t0 = host_t0 + t_begin.elapsed_time(ev[a][0]) * 1e-3
+        t1 = host_t0 + t_begin.elapsed_time(ev[b - 1][2]) * 1e-3
+        mhz = clocks.samples_between(t0 - 0.1, t1 + 0.1) if clocks else []
+        f = statistics.mean(fwd_ms[a:b])
+        med = statistics.median(mhz) if mhz else None
+        bins.append({"steps": [a, b], "forward_ms": f, "sm_mhz_median": med, "clock_samples": len(mhz),
+                     "forward_ms_x_mhz": f * med if med else None})
     ms_step = max_over_ranks(total_ms / args.steps, world)
     # The clock sampler covers the timed steps only: nvidia-smi's queries
     # stall host <-> device copies (the end-to-end loop below ran at 7.2 ms
@@ -482,8 +512,65 @@ def run_gpu(args, wl, world, rank, local):
             frac=prod["achieved_tflops"] / peaks["bf16_tflops"]),
         "gpu_launches": 4 * args.steps,
         "clocks": clocks.summary() if clocks else None,
+        "step_bins": bins,
     }
     return line
+
+
+def time_config(name, steps, warmup, local, peaks):
+    """One other workload: prepare + forward `steps` times on resident inputs,
+    CUDA-event times per launch, its own clock record and roofline line."""
+    import torch
+
+    import frame_aligned_window_gb300 as fw
+    from workloads import WORKLOADS, generate
+
+    wl = WORKLOADS[name]
+    dev = torch.device("cuda", local)
+    q, k, v = (x.to(dev) for x in generate(wl))
+    out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    plan = fw.wsattn_plan(wl.frames, wl.tokens_per_frame, wl.window, wl.ref_frames, wl.heads,
+                          wl.head_dim)
+    flops = step_flops(wl, plan.active_pairs)
+    stream = torch.cuda.current_stream()
+    for _ in range(max(3, warmup)):
+        fw.wsattn_prepare(plan, q, k)
+        fw.wsattn_forward(plan, q, k, v, out)
+    torch.cuda.synchronize()
+    clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.6)
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
+    torch.cuda.synchronize()
+    clocks.mark_start()
+    for e0, e1, e2 in ev:
+        e0.record(stream)
+        fw.wsattn_prepare(plan, q, k)
+        e1.record(stream)
+        fw.wsattn_forward(plan, q, k, v, out)
+        e2.record(stream)
+    torch.cuda.synchronize()
+    clocks.mark_stop()
+    clocks.stop()
+    status = fw.wsattn_device_status(plan)
+    if status != 0:
+        raise RuntimeError(f"{name}: device status {fw.wsattn_status_string(status)}")
+    fwd = statistics.mean(b.elapsed_time(c) for _, b, c in ev)
+    prep = statistics.mean(a.elapsed_time(b) for a, b, _ in ev)
+    step = statistics.mean(a.elapsed_time(c) for a, _, c in ev)
+    achieved = flops / (fwd * 1e-3) / 1e12
+    res = {"workload": wl.label(), "block_k": plan.block_k, "steps": steps,
+           "gflop_per_call": flops / 1e9, "ms_per_forward": fwd, "ms_per_prepare": prep,
+           "ms_per_step": step,
+           "roofline": {"bound": "tensor", "achieved": achieved, "peak": peaks["bf16_tflops"],
+                        "unit": "TFLOP/s", "frac": achieved / peaks["bf16_tflops"],
+                        "peak_source": f"{peaks['source']} (bf16 burst)"},
+           "clocks": clocks.summary()}
+    if name in ("tiny", "small"):
+        res["note"] = "latency-bound: fewer work items than SMs' worth of steps"
+    del q, k, v, out
+    return res
 
 
 def main():
@@ -499,6 +586,8 @@ def main():
                     help="wsattn_produce calls timed after the attention steps (0: none)")
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for the cpu_baseline sample")
+    ap.add_argument("--other-configs", default="sr_long,dense,small,tiny",
+                    help="comma-separated workloads timed after the main one (rank 0, N=1 only)")
     args = ap.parse_args()
     from workloads import WORKLOADS
     wl = WORKLOADS[args.workload]
@@ -507,6 +596,12 @@ def main():
         run_reference(args, wl, world, rank)
         return
     line = run_gpu(args, wl, world, rank, local)
+    if rank == 0 and line is not None and world == 1 and args.other_configs:
+        steps_of = {"sr_long": 30, "dense": 30, "sr": 60, "small": 200, "tiny": 200}
+        line["configs"] = {}
+        for name in [x for x in args.other_configs.split(",") if x and x != wl.name]:
+            line["configs"][name] = time_config(name, steps_of.get(name, 30), args.warmup, local,
+                                                _peaks())
     if rank == 0 and line is not None:
         if not args.no_cpu_baseline and world == 1:
             v, secs, sample, threads = oracle_timing(wl, args.cpu_budget)

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 
 def test_bench_json_line_small():
     cmd = [sys.executable, "bench.py", "--workload", "small", "--steps", "5", "--warmup", "3",
-           "--no-cpu-baseline", "--produce-steps", "2"]
+           "--no-cpu-baseline", "--produce-steps", "2", "--other-configs", "tiny"]
     r = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=600)
     assert r.returncode == 0, r.stderr[-2000:]
     lines = [ln for ln in r.stdout.splitlines() if ln.startswith("{")]
@@ -42,3 +42,13 @@ def test_bench_json_line_small():
     assert d["gpu_launches"] == 4 * d["steps"]
     assert d["produce"]["ms_per_call"] > 0 and 0 < d["produce"]["frac"] < 2
     assert "sm_mhz" in d["clocks"]
+    # step bins cover the timed steps in order
+    bins = d["step_bins"]
+    assert bins[0]["steps"][0] == 0 and bins[-1]["steps"][1] == d["steps"]
+    assert all(b["forward_ms"] > 0 for b in bins)
+    # the other workloads' lines
+    t = d["configs"]["tiny"]
+    assert t["ms_per_forward"] > 0 and t["ms_per_prepare"] > 0
+    assert t["ms_per_forward"] + t["ms_per_prepare"] <= t["ms_per_step"] * 1.001
+    assert abs(t["roofline"]["frac"] - t["roofline"]["achieved"] / t["roofline"]["peak"]) < 1e-9
+    assert "sm_mhz" in t["clocks"]
