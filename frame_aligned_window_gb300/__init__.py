@@ -4,13 +4,16 @@ Argument marshalling only: every step of the computation runs in the CUDA
 library (include/wsattn.h documents each call).  Tensors are torch tensors
 used as device memory; the current torch CUDA stream is passed to the
 library.  If libwsattn.so is missing or fails to load, importing this
-package raises: there is no fallback implementation.
+package raises: there is no fallback implementation.  The environment
+variable WSATTN_LIBRARY names another build of the same library to load
+instead (the tests use it for the bounds-checking libwsattn_debug.so).
 
 The names mirror the C ABI:
     wsattn_plan, wsattn_plan_ex, wsattn_plan_destroy, wsattn_prepare, wsattn_forward,
     wsattn_plan_info, wsattn_get_block_map, wsattn_get_csr, wsattn_get_stats,
     wsattn_plan_set_debug, wsattn_plan_set_bound, wsattn_device_status,
-    wsattn_selftest_timeout, wsattn_status_string, wsattn_prepare_static, wsattn_produce
+    wsattn_selftest_timeout, wsattn_status_string, wsattn_prepare_static, wsattn_produce,
+    wsattn_build_flags
 """
 from __future__ import annotations
 
@@ -20,7 +23,8 @@ import os
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libwsattn.so")
+LIB_PATH = os.environ.get("WSATTN_LIBRARY") or os.path.join(_HERE, "libwsattn.so")
+DEBUG_LIB_PATH = os.path.join(_HERE, "libwsattn_debug.so")
 
 # C ABI entry points declared in include/wsattn.h
 EXPORTS = (
@@ -28,7 +32,7 @@ EXPORTS = (
     "wsattn_plan_info", "wsattn_get_block_map", "wsattn_get_csr", "wsattn_get_stats",
     "wsattn_plan_set_debug", "wsattn_plan_set_bound", "wsattn_device_status",
     "wsattn_selftest_timeout", "wsattn_status_string", "wsattn_prepare_static",
-    "wsattn_produce",
+    "wsattn_produce", "wsattn_build_flags",
 )
 
 # wsattn_bound
@@ -41,7 +45,10 @@ MASK_REF_SUFFIX = 2
 MASK_REF_LOCAL = 4
 
 STATUS = {0: "OK", 1: "BAD_ARG", 2: "BAD_BLOCK", 3: "UNSUPPORTED", 4: "NOT_PREPARED",
-          5: "BATCH_MISMATCH", 6: "CUDA", 7: "TIMEOUT", 8: "NO_MEMORY"}
+          5: "BATCH_MISMATCH", 6: "CUDA", 7: "TIMEOUT", 8: "NO_MEMORY", 9: "BOUNDS"}
+
+# wsattn_build_flags bits
+BUILD_DEBUG = 1
 
 
 class WsattnError(RuntimeError):
@@ -52,7 +59,8 @@ class WsattnError(RuntimeError):
 
 if not os.path.exists(LIB_PATH):
     raise ImportError(f"{LIB_PATH} is missing: build it with "
-                      "`python frame_aligned_window_gb300/build.py`")
+                      "`python frame_aligned_window_gb300/build.py`"
+                      + (" --debug" if LIB_PATH == DEBUG_LIB_PATH else ""))
 _lib = ctypes.CDLL(LIB_PATH)
 
 _P, _I, _F, _SZ = ctypes.c_void_p, ctypes.c_int, ctypes.c_float, ctypes.c_size_t
@@ -72,10 +80,16 @@ _lib.wsattn_selftest_timeout.argtypes = [_I, ctypes.POINTER(_I), _P]
 _lib.wsattn_status_string.argtypes = [_I]
 _lib.wsattn_prepare_static.argtypes = [_I, _I, _I, _I, _F, _P, _P, _P, _P, _P, _P, _P, _P, _P]
 _lib.wsattn_produce.argtypes = [_P, _I, _P, _I, _P, _P, _P, _F, _P, _P, _P, _P]
+_lib.wsattn_build_flags.argtypes = []
 _lib.wsattn_status_string.restype = ctypes.c_char_p
 for _name in EXPORTS:
     if _name != "wsattn_status_string":
         getattr(_lib, _name).restype = _I
+
+
+def wsattn_build_flags() -> int:
+    """BUILD_DEBUG when the loaded library checks bounds in its kernels."""
+    return int(_lib.wsattn_build_flags())
 
 
 def status_text(code: int) -> str:

@@ -509,13 +509,14 @@ int wsattn_device_status(wsattn_plan_t plan, void* stream) {
   if (cudaMemcpy(&st, plan->d_status, sizeof(int), cudaMemcpyDeviceToHost) != cudaSuccess)
     return WSATTN_ERR_CUDA;
   if (st == 0) return WSATTN_OK;
+  const int code = (st & wsattn::kStatusBounds) ? WSATTN_ERR_BOUNDS : WSATTN_ERR_TIMEOUT;
   // A forward that gave up on a wait may leave its work counters non-zero
   // (the last CTA to finish resets them); the next forward would then skip
   // items.  Reset them with the status word.
   if (cudaMemset(plan->d_status, 0, sizeof(int)) != cudaSuccess ||
       (plan->d_work && cudaMemset(plan->d_work, 0, 2 * sizeof(int)) != cudaSuccess))
     return WSATTN_ERR_CUDA;
-  return WSATTN_ERR_TIMEOUT;
+  return code;
 }
 
 int wsattn_selftest_timeout(int limit_ms, int* status, void* stream) {
@@ -542,6 +543,8 @@ int wsattn_selftest_timeout(int limit_ms, int* status, void* stream) {
   return rc;
 }
 
+int wsattn_build_flags(void) { return wsattn::kDebugBuild ? WSATTN_BUILD_DEBUG : 0; }
+
 const char* wsattn_status_string(int status) {
   switch (status) {
     case WSATTN_OK: return "ok";
@@ -553,6 +556,7 @@ const char* wsattn_status_string(int status) {
     case WSATTN_ERR_CUDA: return "CUDA runtime error";
     case WSATTN_ERR_TIMEOUT: return "device-side wait expired";
     case WSATTN_ERR_NO_MEMORY: return "host allocation failed";
+    case WSATTN_ERR_BOUNDS: return "device bounds check failed (debug build)";
     default: return "unknown status";
   }
 }

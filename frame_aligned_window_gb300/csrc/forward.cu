@@ -351,13 +351,20 @@ __device__ void producer_qk(const FwdParams& p, const Shared& s) {
     if (it == -2) return drain();
     if (it < 0) break;
     const Item im = map_item(p, it);
+    if (!WSATTN_BOUNDS(p.status, im.tile >= 0 && im.tile < p.n_tiles && im.bh >= 0 &&
+                                     im.bh < p.bh))
+      return;
     const WorkTile t = p.tiles[im.tile];
     const int y0 = im.bh * p.n;
+    [[maybe_unused]] const int rows = p.bh * p.n;
     if (!wait(s, bar(s, B_QEMPTY), (qc & 1u) ^ 1u, kStatusTimeoutProducer)) return drain();
     mbar_arrive_expect_tx(bar(s, B_QFULL), kTileM * D * 2);
+    if (WSATTN_BOUNDS(p.status, t.row0 >= 0 && t.nvalid > 0 && t.nvalid <= kTileM &&
+                                    t.row0 + t.nvalid <= p.n)) {
 #pragma unroll
-    for (int c = 0; c < kBoxes; ++c)
-      tma_load_2d(s.q + c * (kTileM * 128), &p.tm_q, bar(s, B_QFULL), c * 64, y0 + t.row0);
+      for (int c = 0; c < kBoxes; ++c)
+        tma_load_2d(s.q + c * (kTileM * 128), &p.tm_q, bar(s, B_QFULL), c * 64, y0 + t.row0);
+    }
     ++qc;
     Steps ks;
     ks.init(t);
@@ -369,8 +376,13 @@ __device__ void producer_qk(const FwdParams& p, const Shared& s) {
       const uint32_t fb = bar(s, B_KFULL0 + kr.slot);
       mbar_arrive_expect_tx(fb, stage_bytes);
       const uint32_t dst = s.k + kr.slot * stage_bytes;
+      // the step's keys lie in the head (rows past them, to the box end, are
+      // loaded but never read)
+      if (WSATTN_BOUNDS(p.status, nb >= 1 && nb <= G && row >= y0 && row + nb * bk <= y0 + p.n &&
+                                      row + nb * bk <= rows)) {
 #pragma unroll
-      for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_k, fb, c * 64, row);
+        for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_k, fb, c * 64, row);
+      }
       kph = (kph & ~(1u << kr.slot)) | (kr.phase << kr.slot);
       kiss |= 1u << kr.slot;
       kr.next(nk);
@@ -395,6 +407,9 @@ __device__ void producer_v(const FwdParams& p, const Shared& s) {
     if (it == -2) return drain();
     if (it < 0) break;
     const Item im = map_item(p, it);
+    if (!WSATTN_BOUNDS(p.status, im.tile >= 0 && im.tile < p.n_tiles && im.bh >= 0 &&
+                                     im.bh < p.bh))
+      return;
     const WorkTile t = p.tiles[im.tile];
     const int y0 = im.bh * p.n;
     Steps vs;
@@ -407,8 +422,10 @@ __device__ void producer_v(const FwdParams& p, const Shared& s) {
       const uint32_t fb = bar(s, B_VFULL0 + vr.slot);
       mbar_arrive_expect_tx(fb, stage_bytes);
       const uint32_t dst = s.v + vr.slot * stage_bytes;
+      if (WSATTN_BOUNDS(p.status, nb >= 1 && nb <= G && row >= y0 && row + nb * bk <= y0 + p.n)) {
 #pragma unroll
-      for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_v, fb, c * 64, row);
+        for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_v, fb, c * 64, row);
+      }
       vph = (vph & ~(1u << vr.slot)) | (vr.phase << vr.slot);
       viss |= 1u << vr.slot;
       vr.next(nv);
@@ -467,9 +484,15 @@ __device__ void qk_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
       tc_fence_after();
       const uint64_t kd = kdesc0 + slot * stage16;
       const uint32_t id = id_qk0 | ((keys >> 3) << 17);
+      // S (keys columns) and Q (D/2 columns) inside the allocation, N a
+      // multiple of 16 no larger than a step, the K stage inside its ring
+      if (WSATTN_BOUNDS(p.status, keys >= 16 && keys % 16 == 0 && keys <= static_cast<uint32_t>(ns) &&
+                                      tc_.s + keys <= kTmemCols && tc_.q + D / 2 <= kTmemCols &&
+                                      slot < nk)) {
 #pragma unroll
-      for (int kk = 0; kk < D / 16; ++kk)
-        mma_ts_warp(t_s, t_q + kk * 8, kd + (kk / 4) * box16 + (kk % 4) * 2, id, kk > 0 ? 1u : 0u);
+        for (int kk = 0; kk < D / 16; ++kk)
+          mma_ts_warp(t_s, t_q + kk * 8, kd + (kk / 4) * box16 + (kk % 4) * 2, id, kk > 0 ? 1u : 0u);
+      }
       tc_commit_warp(bar(s, B_KEMPTY0 + slot));
       tc_commit_warp(bar(s, B_SFULL));
       kr.next(nk);
@@ -515,11 +538,17 @@ __device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
       tc_fence_after();
       const uint64_t vd = vdesc0 + vslot * stage16;
       const uint32_t a_p = t_p + pb * tc_.pstride;
-      // 16 key rows (2 KB of V, 8 P columns) per k-step
-      mma_ts_warp(t_o, a_p, vd, id_pv, j > 0 ? 1u : 0u);
+      // P (8 columns per k-step) and O (D columns) inside the allocation,
+      // the V stage inside its ring, the k-steps inside the unrolled range
+      if (WSATTN_BOUNDS(p.status, nks >= 1 && nks <= kNumWG * MAXC &&
+                                      tc_.p + pb * tc_.pstride + 8u * nks <= kTmemCols &&
+                                      tc_.o + D <= kTmemCols && vslot < nv)) {
+        // 16 key rows (2 KB of V, 8 P columns) per k-step
+        mma_ts_warp(t_o, a_p, vd, id_pv, j > 0 ? 1u : 0u);
 #pragma unroll
-      for (int kk = 1; kk < kNumWG * MAXC; ++kk)
-        if (kk < nks) mma_ts_warp(t_o, a_p + kk * 8, vd + kk * 128, id_pv, 1u);
+        for (int kk = 1; kk < kNumWG * MAXC; ++kk)
+          if (kk < nks) mma_ts_warp(t_o, a_p + kk * 8, vd + kk * 128, id_pv, 1u);
+      }
       tc_commit_warp(bar(s, B_VEMPTY0 + vslot));
       tc_commit_warp(bar(s, B_PVDONE0 + pb));
       vr.next(nv);
@@ -634,8 +663,9 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
     const Item im = map_item(p, it);
     const WorkTile t = p.tiles[im.tile];
     const bool online = p.force_path >= 0 ? (p.force_path == 1) : (p.elig[im.bh] == 0);
-    const bool valid = r < t.nvalid;
     const size_t grow = static_cast<size_t>(im.bh) * p.n + t.row0 + r;
+    const bool valid =
+        r < t.nvalid && WSATTN_BOUNDS(p.status, grow < static_cast<size_t>(p.bh) * p.n);
     Steps st;
     st.init(t);
     float l = 0.f;
@@ -653,18 +683,24 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         int f16, n16;  // this warpgroup's 16-column chunks of the step
         wg_share(keys / 16, wg, f16, n16);
         const uint32_t c0 = static_cast<uint32_t>(16 * f16);  // first S column
+        const uint32_t pb = pr.slot;
+        // the S columns read and the P columns written lie in the allocation
+        // and P stays inside its own buffer
+        const bool cols_ok = WSATTN_BOUNDS(
+            p.status, tc_.s + c0 + 16u * MAXC <= kTmemCols && n16 <= MAXC &&
+                          c0 / 2 + 8u * n16 <= tc_.pstride && tc_.p + 2u * tc_.pstride <= kTmemCols);
         if (!wait_warp(s, bar(s, B_SFULL), su)) return;
         tc_fence_after();
         uint32_t sv[MAXC][16];
-        load_s<MAXC>(lane + tc_.s + c0, sv);
+        if (cols_ok) load_s<MAXC>(lane + tc_.s + c0, sv);
         tc_fence_before();
         warp_arrive(bar(s, B_SEMPTY));
         su ^= 1u;
         // the PV that read this P buffer two steps back must be done
-        const uint32_t pb = pr.slot;
         if (!wait_warp(s, bar(s, B_PVDONE0 + pb), pr.phase ^ 1u)) return;
         tc_fence_after();
-        exp_chunks<MAXC>(sv, n16, c2, nb2, la, lb, lane + tc_.p + pb * tc_.pstride + c0 / 2);
+        if (cols_ok)
+          exp_chunks<MAXC>(sv, n16, c2, nb2, la, lb, lane + tc_.p + pb * tc_.pstride + c0 / 2);
         tmem_wait_st();
         tc_fence_before();
         warp_arrive(bar(s, B_PFULL0 + pb));
@@ -680,10 +716,21 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         int f16, n16;
         wg_share(keys / 16, wg, f16, n16);
         const uint32_t c0 = static_cast<uint32_t>(16 * f16);
+        const bool cols_ok = WSATTN_BOUNDS(
+            p.status, tc_.s + c0 + 16u * MAXC <= kTmemCols && n16 <= MAXC &&
+                          c0 / 2 + 8u * n16 <= tc_.pstride && tc_.p + 2u * tc_.pstride <= kTmemCols &&
+                          ocol + 16u * nog <= kTmemCols);
         if (!wait_warp(s, bar(s, B_SFULL), su)) return;
         tc_fence_after();
         uint32_t sv[MAXC][16];
-        load_s<MAXC>(lane + tc_.s + c0, sv);
+        if (cols_ok) {
+          load_s<MAXC>(lane + tc_.s + c0, sv);
+        } else {
+#pragma unroll
+          for (int k = 0; k < MAXC; ++k)
+#pragma unroll
+            for (int i = 0; i < 16; ++i) sv[k][i] = 0u;
+        }
         tc_fence_before();
         warp_arrive(bar(s, B_SEMPTY));
         su ^= 1u;
@@ -713,12 +760,13 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         if (!wait_warp(s, bar(s, B_PVDONE0 + pb), pr.phase ^ 1u)) return;
         tc_fence_after();
         uint64_t sa2 = f2_pack(0.f, 0.f), sb2 = sa2;
-        exp_chunks<MAXC>(sv, n16, c2, f2_pack(-m_new, -m_new), sa2, sb2,
-                         lane + tc_.p + pb * tc_.pstride + c0 / 2);
+        if (cols_ok)
+          exp_chunks<MAXC>(sv, n16, c2, f2_pack(-m_new, -m_new), sa2, sb2,
+                           lane + tc_.p + pb * tc_.pstride + c0 / 2);
         const float2 a = f2_unpack(f2_add(sa2, sb2));
         l = l * alpha + (a.x + a.y);
         m = m_new;
-        if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f)) {
+        if (j > 0 && __any_sync(0xffffffffu, alpha < 1.f) && cols_ok) {
           // O += P(j-1) V must have landed before O is rescaled: PV(j-1)
           // read the other P buffer, whose PV-done barrier is at most one
           // use behind (its next use needs P(j+1)), so one parity wait is
@@ -777,11 +825,15 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
     // different bank groups.  Warps of a frame's tail tile store their valid
     // rows themselves.
     const int wq = warp & 3;
-    const bool warp_full = 32 * wq + 32 <= t.nvalid;
+    // O's columns lie in the allocation; a full warp's 32 rows in the output
+    const bool o_ok = WSATTN_BOUNDS(p.status, ocol + 16u * nog <= kTmemCols);
+    const bool warp_full =
+        32 * wq + 32 <= t.nvalid &&
+        WSATTN_BOUNDS(p.status, im.bh * p.n + t.row0 + 32 * wq + 32 <= p.bh * p.n);
     const uint32_t chunk = s.ostage + static_cast<uint32_t>(warp - kSoftmaxWarp0) * kOChunkBytes;
     const int lid = threadIdx.x & 31;
 #pragma unroll 1
-    for (int k = 0; k < nog; ++k) {
+    for (int k = 0; k < (o_ok ? nog : 0); ++k) {
       uint32_t v[16];
       tmem_ld16(lane + ocol + k * 16, v);
       tmem_wait_ld16(v);
@@ -879,8 +931,22 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
   tc_fence_after();
   const uint32_t tbase = *tslot;
   griddep_wait();  // the row maxima and eligibility come from the kernel before
+#ifdef WSATTN_DEBUG
+  uint32_t dsmem = 0;
+  asm volatile("mov.u32 %0, %%dynamic_smem_size;" : "=r"(dsmem));
+  // the shared-memory layout fits the launch's dynamic shared memory, the
+  // rings are at most 4 deep (the barriers there are), the tensor-memory
+  // layout fits the allocation
+  const bool layout_ok = WSATTN_BOUNDS(
+      p.status, (s.ostage + kOStageBytes) - raw <= dsmem && p.stages_k >= 1 && p.stages_k <= 4 &&
+                    p.stages_v >= 1 && p.stages_v <= 4 &&
+                    tmem_cols<D>(p.G * p.bk).q + D / 2 <= kTmemCols);
+#else
+  constexpr bool layout_ok = true;
+#endif
 
-  if (warp == 0) {
+  if (!layout_ok) {
+  } else if (warp == 0) {
     if (lane == 0) producer_qk<D>(p, s);
   } else if (warp == 2) {
     if (lane == 0) producer_v<D>(p, s);

@@ -215,5 +215,24 @@ constexpr int kStatusTimeoutProducer = 1;
 constexpr int kStatusTimeoutMma = 2;
 constexpr int kStatusTimeoutSoftmax = 4;
 constexpr int kStatusTimeoutSelftest = 8;
+constexpr int kStatusBounds = 16;  // a debug build's bounds check failed
+
+// Bounds checks of the debug build (compiled with -DWSATTN_DEBUG): each
+// TMA coordinate, tensor-memory column range, shared-memory layout, output
+// row and work-item index the kernels use is checked against its limit
+// before the access.  A failed check sets kStatusBounds in the status word
+// and the access is skipped; nothing traps.  Release builds compile the
+// checks out (the condition is not evaluated).
+#ifdef WSATTN_DEBUG
+constexpr bool kDebugBuild = true;
+__device__ __forceinline__ bool bounds_ok(int* status, bool ok) {
+  if (!ok && status) atomicOr(status, kStatusBounds);
+  return ok;
+}
+#define WSATTN_BOUNDS(status, cond) (::wsattn::bounds_ok((status), (cond)))
+#else
+constexpr bool kDebugBuild = false;
+#define WSATTN_BOUNDS(status, cond) (true)
+#endif
 
 }  // namespace wsattn

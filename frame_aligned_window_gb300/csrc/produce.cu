@@ -237,7 +237,11 @@ __device__ void p_epilogue(const ProdParams& p, const PShared& s, int total, uin
     if (!__all_sync(0xffffffffu, ok)) return;
     tc_fence_after();
     const int tok = tl.mt * kProdTileM + r;
-    const bool valid = tok < p.n;
+    // the tile lies in the problem: batch element, token tile, feature tile
+    const bool tile_ok = WSATTN_BOUNDS(p.status, tl.b >= 0 && tl.b < p.batch && tl.mt >= 0 &&
+                                                     tl.mt < p.mtiles && tl.nt >= 0 &&
+                                                     tl.nt < p.ntiles);
+    const bool valid = tok < p.n && tile_ok;
     const float inv = valid ? p.inv_rms[static_cast<size_t>(tl.b) * p.n + tok] : 0.f;
     const int f0 = tl.nt * BN;
     const int kind = f0 / hd;  // 0 q, 1 k, 2 v
@@ -278,7 +282,11 @@ __device__ void p_epilogue(const ProdParams& p, const PShared& s, int total, uin
       uint32_t pk[32];
 #pragma unroll
       for (int i = 0; i < 32; ++i) pk[i] = bf16x2(y[2 * i], y[2 * i + 1]);
-      if (kind == 1) {
+      const size_t slot = (static_cast<size_t>(tl.b) * p.heads + h) * p.nparts +
+                          static_cast<size_t>(tl.mt) * 4 + wq;
+      if (kind == 1 && tile_ok &&
+          WSATTN_BOUNDS(p.status, h >= 0 && h < p.heads && d0 + 64 <= D &&
+                                      slot < static_cast<size_t>(p.batch) * p.heads * p.nparts)) {
         // sums of the stored (rounded) keys; rows past N hold zeros
         float a[64];
 #pragma unroll
@@ -287,11 +295,9 @@ __device__ void p_epilogue(const ProdParams& p, const PShared& s, int total, uin
           a[2 * i + 1] = __uint_as_float(pk[i] & 0xFFFF0000u);
         }
         const float2 cs = warp_colsum64(a);
-        const size_t slot = (static_cast<size_t>(tl.b) * p.heads + h) * p.nparts +
-                            static_cast<size_t>(tl.mt) * 4 + wq;
         reinterpret_cast<float2*>(p.part_sum + slot * D + d0)[lane] = cs;
       }
-      if (any_row) {
+      if (any_row && tile_ok && WSATTN_BOUNDS(p.status, kind >= 0 && kind < 3 && h < p.heads)) {
         // 128-byte swizzle: 16-byte unit u of row l sits at unit u ^ (l & 7)
         const uint32_t buf = s.ostage + (static_cast<uint32_t>(wq) * 2 + ob) * kPOutChunk;
         if (lane == 0) bulk_wait_read_1();  // this buffer's previous store has read it

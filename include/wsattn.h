@@ -57,7 +57,9 @@ enum wsattn_status {
   WSATTN_ERR_BATCH_MISMATCH = 5, /* forward batch differs from the last prepare's */
   WSATTN_ERR_CUDA = 6,           /* a CUDA runtime call failed (launch, copy, alloc) */
   WSATTN_ERR_TIMEOUT = 7,        /* a device-side wait expired; results are invalid */
-  WSATTN_ERR_NO_MEMORY = 8       /* host allocation failed */
+  WSATTN_ERR_NO_MEMORY = 8,      /* host allocation failed */
+  WSATTN_ERR_BOUNDS = 9          /* debug build only: a device bounds check failed (the
+                                    access was skipped); results are invalid */
 };
 
 typedef struct wsattn_plan_s* wsattn_plan_t;
@@ -279,7 +281,8 @@ enum wsattn_bound {
  */
 int wsattn_plan_set_bound(wsattn_plan_t plan, int mode);
 
-/* Synchronises `stream` and reports the plan's device status word: OK, or
+/* Synchronises `stream` and reports the plan's device status word: OK,
+ * BOUNDS if a debug build's bounds check failed (see wsattn_build_flags), or
  * TIMEOUT if a device-side wait of a kernel launched with this plan expired
  * (the word is then cleared, and so are the plan's forward work counters,
  * which a forward that gave up may have left mid-count).  CUDA if the
@@ -291,6 +294,16 @@ int wsattn_device_status(wsattn_plan_t plan, void* stream);
  * milliseconds, and reports the status the kernel wrote (TIMEOUT expected)
  * in *status.  Synchronises `stream`.  Returns CUDA if the launch failed. */
 int wsattn_selftest_timeout(int limit_ms, int* status, void* stream);
+
+/* Build flags of the loaded library: bit 0 (WSATTN_BUILD_DEBUG) is set in a
+ * build compiled with WSATTN_DEBUG, whose kernels check every TMA
+ * coordinate, tensor-memory column range, shared-memory layout, output row
+ * and work-item index against its limit before the access; a failed check
+ * skips the access and sets a status bit that wsattn_device_status reports
+ * as BOUNDS (no trap, no assert).  The paper has no counterpart: it is a
+ * test aid standing in for a memory checker.  Release builds return 0. */
+enum { WSATTN_BUILD_DEBUG = 1 };
+int wsattn_build_flags(void);
 
 /* Static text for a status code. */
 const char* wsattn_status_string(int status);

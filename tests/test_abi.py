@@ -187,3 +187,11 @@ def test_produce_argument_errors_without_device_work():
     # H * D = 64 is not a multiple of 128
     small = fw.wsattn_plan(4, 48, 1, 1, 1, 64)
     assert produce(small.handle, 1, a, 64, a, a, a, f(1e-6), a, a, a, None) == 3
+
+
+def test_release_library_reports_no_debug_flag():
+    import frame_aligned_window_gb300 as fw
+    if os.environ.get("WSATTN_LIBRARY"):
+        pytest.skip("another build of the library is loaded")
+    assert fw.wsattn_build_flags() == 0
+    assert fw.wsattn_status_string(9) == "device bounds check failed (debug build)"
