@@ -166,13 +166,15 @@ int ensure_workspace(wsattn_plan_s* p, int batch, cudaStream_t stream) {
   const size_t frame_slots = static_cast<size_t>(BH) * (hp.F + hp.R);
   if (slots < frame_slots) slots = frame_slots;
   auto up = [](size_t x) { return (x + 255) / 256 * 256; };
-  const size_t n_b = up(sizeof(float) * BH * hp.N);  // b_rows, and again for m_rows
+  const size_t n_b = up(sizeof(float) * BH * hp.N);  // qn_rows, and again for c_rows
   const size_t n_mu = up(sizeof(float) * BH * hp.D);
   const size_t n_h = up(sizeof(float) * BH);
   const size_t n_el = up(BH);
   const size_t n_ps = up(sizeof(float) * slots * hp.D);
   const size_t n_pm = up(sizeof(float) * slots);
-  const size_t total = 2 * n_b + n_mu + 2 * n_h + n_el + n_ps + 2 * n_pm;
+  const size_t n_kq = up(sizeof(float) * BH * (hp.F + hp.R));
+  const size_t n_cnt = up(sizeof(int) * BH);
+  const size_t total = 2 * n_b + n_mu + 2 * n_h + n_el + n_ps + 2 * n_pm + n_kq + n_cnt;
   if (p->ws) {
     if (cudaStreamSynchronize(stream) != cudaSuccess) return WSATTN_ERR_CUDA;
     cudaFree(p->ws);
@@ -185,17 +187,23 @@ int ensure_workspace(wsattn_plan_s* p, int batch, cudaStream_t stream) {
   }
   char* c = static_cast<char*>(p->ws);
   PrepBuffers& b = p->buf;
-  b.b_rows = reinterpret_cast<float*>(c); c += n_b;
-  b.m_rows = reinterpret_cast<float*>(c); c += n_b;
+  b.qn_rows = reinterpret_cast<float*>(c); c += n_b;
+  b.c_rows = reinterpret_cast<float*>(c); c += n_b;
   b.mu = reinterpret_cast<float*>(c); c += n_mu;
   b.kmax = reinterpret_cast<float*>(c); c += n_h;
   b.bmax = reinterpret_cast<float*>(c); c += n_h;
   b.elig = reinterpret_cast<uint8_t*>(c); c += n_el;
   b.part_sum = reinterpret_cast<float*>(c); c += n_ps;
   b.part_kmax = reinterpret_cast<float*>(c); c += n_pm;
-  b.part_qmax = reinterpret_cast<float*>(c);
+  b.part_qmax = reinterpret_cast<float*>(c); c += n_pm;
+  b.kq = reinterpret_cast<float*>(c); c += n_kq;
+  b.head_count = reinterpret_cast<int*>(c);
+  b.nfq = hp.F + hp.R;
+  b.tq = hp.T;
   b.nchunk = nchunk;
   b.rows_per_chunk = rpc;
+  // pass B's per-head counters start at zero (each launch leaves them so)
+  if (cudaMemsetAsync(b.head_count, 0, n_cnt, stream) != cudaSuccess) return WSATTN_ERR_CUDA;
   p->ws_batch = batch;
   p->prepared_batch = 0;
   return WSATTN_OK;
@@ -401,7 +409,12 @@ int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, 
   prm.tiles = plan->d_tiles;
   prm.cls = plan->d_cls;
   prm.n_cls = static_cast<int>(hp.cls.size()) - 1;
-  prm.m_rows = plan->buf.m_rows;
+  prm.qn_rows = plan->buf.qn_rows;
+  prm.c_rows = plan->buf.c_rows;
+  prm.kq = plan->buf.kq;
+  prm.nfq = plan->buf.nfq;
+  prm.tq = static_cast<int>(plan->buf.tq);
+  prm.scale = 1.0f / std::sqrt(static_cast<float>(hp.D));
   prm.elig = plan->buf.elig;
   prm.out = out;
   prm.status = plan->d_status;
@@ -468,12 +481,24 @@ int wsattn_get_stats(wsattn_plan_t plan, float* b_rows, float* m_rows, float* mu
   const HostPlan& hp = plan->hp;
   const size_t BH = static_cast<size_t>(plan->prepared_batch) * hp.H;
   const PrepBuffers& b = plan->buf;
-  if (b_rows && cudaMemcpy(b_rows, b.b_rows, BH * hp.N * sizeof(float),
-                           cudaMemcpyDeviceToHost) != cudaSuccess)
-    return WSATTN_ERR_CUDA;
-  if (m_rows && cudaMemcpy(m_rows, b.m_rows, BH * hp.N * sizeof(float),
-                           cudaMemcpyDeviceToHost) != cudaSuccess)
-    return WSATTN_ERR_CUDA;
+  if (b_rows || m_rows) {
+    // b_i and m_i are formed from what prepare keeps (||q_i||, c_i, the
+    // frame bounds) by a small kernel, into a temporary buffer
+    const size_t rows = BH * hp.N;
+    float* tmp = nullptr;
+    if (cudaMalloc(&tmp, 2 * rows * sizeof(float)) != cudaSuccess) return WSATTN_ERR_CUDA;
+    const float scale = 1.0f / std::sqrt(static_cast<float>(hp.D));
+    bool ok = wsattn::launch_finalize_rows(b, static_cast<int>(BH), hp.N, scale, tmp, tmp + rows,
+                                           nullptr) == cudaSuccess &&
+              cudaDeviceSynchronize() == cudaSuccess;
+    if (ok && b_rows)
+      ok = cudaMemcpy(b_rows, tmp, rows * sizeof(float), cudaMemcpyDeviceToHost) == cudaSuccess;
+    if (ok && m_rows)
+      ok = cudaMemcpy(m_rows, tmp + rows, rows * sizeof(float), cudaMemcpyDeviceToHost) ==
+           cudaSuccess;
+    cudaFree(tmp);
+    if (!ok) return WSATTN_ERR_CUDA;
+  }
   if (mu && cudaMemcpy(mu, b.mu, BH * hp.D * sizeof(float), cudaMemcpyDeviceToHost) != cudaSuccess)
     return WSATTN_ERR_CUDA;
   if (kmax && cudaMemcpy(kmax, b.kmax, BH * sizeof(float), cudaMemcpyDeviceToHost) != cudaSuccess)

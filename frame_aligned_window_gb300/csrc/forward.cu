@@ -651,6 +651,11 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
   const uint32_t ocol = tc_.o + static_cast<uint32_t>(16 * og0);
   const float c = p.scale_log2;
   const uint64_t c2 = f2_pack(c, c);
+  // The output is not read again here: its L2 lines go first, so they are
+  // written back while this kernel runs (it does not bind on DRAM) instead
+  // of during the next call's statistics passes, whose reads would evict
+  // them.
+  const uint64_t out_policy = policy_evict_first();
   uint32_t qc = 0, tiles_done = 0, xpar = 0, xc = 0;
   uint32_t su = 0;  // parity of the current use of S
   Ring pr;          // P buffer
@@ -670,7 +675,13 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
     st.init(t);
     float l = 0.f;
     float m = -INFINITY;
-    const float nb_fixed = valid ? -p.m_rows[grow] * kLog2e : 0.f;
+    // the row's fixed max m_i = b_i + c_i, b_i = (scale ||q_i||) K of its frame
+    const float nb_fixed =
+        valid ? -__fadd_rn(row_bound(p.scale, p.qn_rows[grow],
+                                     p.kq[static_cast<size_t>(im.bh) * p.nfq + t.row0 / p.tq]),
+                           p.c_rows[grow]) *
+                    kLog2e
+              : 0.f;
     if (!online) {
       // Fixed max: every step is load, exp, pack, store; the row sum
       // accumulates.
@@ -851,16 +862,17 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         fence_proxy_async_smem();
         __syncwarp();
         if (lid == 0) {
-          tma_store_2d(&p.tm_o, chunk, 16 * (og0 + k), im.bh * p.n + t.row0 + 32 * wq);
+          tma_store_2d_hint(&p.tm_o, chunk, 16 * (og0 + k), im.bh * p.n + t.row0 + 32 * wq,
+                            out_policy);
           bulk_commit_group();
         }
       } else if (valid) {
         float4* dst = reinterpret_cast<float4*>(orow + k * 16);
 #pragma unroll
         for (int i = 0; i < 4; ++i)
-          dst[i] = make_float4(__uint_as_float(v[4 * i]) * inv, __uint_as_float(v[4 * i + 1]) * inv,
-                               __uint_as_float(v[4 * i + 2]) * inv,
-                               __uint_as_float(v[4 * i + 3]) * inv);
+          st_global_v4_hint(dst + i, __uint_as_float(v[4 * i]) * inv,
+                            __uint_as_float(v[4 * i + 1]) * inv, __uint_as_float(v[4 * i + 2]) * inv,
+                            __uint_as_float(v[4 * i + 3]) * inv, out_policy);
       }
     }
     if (nxt < 0) break;

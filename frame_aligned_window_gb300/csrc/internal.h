@@ -84,9 +84,18 @@ __host__ __device__ inline bool frames_interact(int a, int c, int F, int w, int 
 int auto_block(int T);
 
 // ------------------------------------------------------------ prepare
+// What prepare leaves on the device: per row ||q_i|| and c_i = scale q_i.mu,
+// per (b, h) and query frame the key-norm bound K (the head's K_h, or the
+// window's), and per (b, h) K_h, B_h and eligibility.  The row bound and the
+// fixed max follow as b_i = (scale ||q_i||) K and m_i = b_i + c_i (the
+// forward forms m_i when it starts a tile; finalize_rows writes both out for
+// readers).
 struct PrepBuffers {
-  float* b_rows;        // [BH * N] bound b_i; holds ||q_i|| between passes
-  float* m_rows;        // [BH * N] fixed max m_i = b_i + scale q_i.mu; holds c_i between passes
+  float* qn_rows;       // [BH * N] ||q_i||
+  float* c_rows;        // [BH * N] c_i = scale q_i.mu
+  float* kq;            // [BH * nfq] key-norm bound of each query frame
+  int nfq;              // query frames per head (1 when the head is one frame)
+  int64_t tq;           // rows per query frame
   float* mu;            // [BH * D]
   float* kmax;          // [BH]
   float* bmax;          // [BH]
@@ -94,6 +103,7 @@ struct PrepBuffers {
   float* part_sum;      // [BH * nchunk * D]
   float* part_kmax;     // [BH * nchunk]
   float* part_qmax;     // [BH * nchunk]
+  int* head_count;      // [BH] pass B chunks finished per head (0 between launches)
   int nchunk;
   int rows_per_chunk;
 };
@@ -108,14 +118,28 @@ struct FrameWindow {
   int flags;  // wsattn_mask_flags
 };
 
-// Enqueues the three prepare passes; returns a cudaError_t.  With `win`
-// non-null the chunks must be the frames and the row bounds use the
-// per-window key-norm maximum.  With `key_sums` non-null ([BH,
-// kKeySumRows, D]: each head's key column sums in kKeySumRows partial rows,
-// from the producer) pass A is skipped.
+// Enqueues the prepare passes (A: key column sums; B: mean, norms, and in
+// each head's last CTA the per-frame bounds, B_h and eligibility); returns a
+// cudaError_t.  With `win` non-null the chunks must be the frames and the
+// bounds are the per-window key-norm maxima (buf.nfq = frames).  With
+// `key_sums` non-null ([BH, kKeySumRows, D]: each head's key column sums in
+// kKeySumRows partial rows, from the producer) pass A is skipped.
 cudaError_t launch_prepare(const void* q, const void* k, int BH, int64_t N, int D, float scale,
                            float tau, const PrepBuffers& buf, const FrameWindow* win,
                            const float* key_sums, cudaStream_t stream);
+
+// b_i = (scale ||q_i||) K and m_i = b_i + c_i for every row, from what
+// prepare left in `buf`, into b_out and m_out ([BH * N]; they may be
+// buf.qn_rows and buf.c_rows themselves).  For readers of the statistics;
+// the forward forms m_i itself.
+cudaError_t launch_finalize_rows(const PrepBuffers& buf, int BH, int64_t N, float scale,
+                                 float* b_out, float* m_out, cudaStream_t stream);
+
+// The row bound and fixed max exactly as every kernel forms them (rounded
+// products, no contraction), so readers see the values the forward uses.
+__device__ __forceinline__ float row_bound(float scale, float qn, float k) {
+  return __fmul_rn(__fmul_rn(scale, qn), k);
+}
 
 // Chunking of the N rows of one head across CTAs.
 void prepare_chunking(int BH, int64_t N, int num_sms, int* nchunk, int* rows_per_chunk);
@@ -130,7 +154,12 @@ struct FwdParams {
   const int32_t* cls;    // class boundaries into tiles, n_cls + 1 entries
   int* work;             // [2]: next work item, CTAs finished (both 0 between launches)
   int n_cls;
-  const float* m_rows;   // [BH*N] fixed softmax max per row (uncentered logit units)
+  const float* qn_rows;  // [BH*N] ||q_i||
+  const float* c_rows;   // [BH*N] c_i = scale q_i.mu
+  const float* kq;       // [BH * nfq] key-norm bound per query frame
+  int nfq;               // query frames per head
+  int tq;                // rows per query frame
+  float scale;           // softmax scale
   const uint8_t* elig;   // [BH]
   float* out;            // [BH*N, D]
   int* status;           // device status word (bit set on an expired wait)

@@ -15,19 +15,23 @@
 // m_i = b_i + c_i.  The forward kernel multiplies the caller's bf16 keys as
 // they are (no second rounding of k - mu) and uses m_i as the row's fixed max.
 //
-// Three HBM-bound passes over [BH, N, D] bf16, each CTA owning one chunk of
-// rows of one (b, h); every reduction runs in a fixed order (no atomics), so
-// the results are bit-reproducible:
+// Two HBM-bound passes over [BH, N, D] bf16, each CTA owning one chunk of
+// rows of one (b, h); every reduction runs in a fixed order, so the results
+// are bit-reproducible:
 //   A  per-chunk key column sums                                (reads k)
 //   B  mu = ordered sum of the chunk sums / N; key norms ||k_j - mu|| and
 //      their per-chunk max; query norms ||q_i||, c_i, per-chunk max query
-//      norm (row norms reduced with warp shuffles)        (reads k and q)
-//   C  K_h = max of the chunk maxima (with window bounds, where the chunks
-//      are the frames: the max over the frames the row's frame attends);
-//      b_i = (scale ||q_i||) K_h;
-//      m_i = b_i + c_i; B_h = (scale max ||q_i||) K_h, which equals max_i b_i
-//      because the expression is monotone in ||q_i||;
+//      norm (row norms reduced with warp shuffles)        (reads k and q).
+//      The last CTA of each head to finish (a per-head counter) then takes
+//      K_h = max of the chunk maxima (with window bounds, where the chunks
+//      are the frames: for each query frame, the max over the frames it
+//      attends), B_h = (scale max ||q_i||) K_h, which equals max_i b_i because
+//      the expression is monotone in ||q_i||, and
 //      eligible = B_h <= tau and 2 B_h < 126 ln 2.
+// The row bound b_i = (scale ||q_i||) K and the fixed max m_i = b_i + c_i are
+// not written out on the hot path: the forward forms m_i from ||q_i||, c_i
+// and its frame's K when it starts a tile.  finalize_rows writes b_i and m_i
+// for the readers of the statistics.
 #include <cuda_bf16.h>
 
 #include "internal.h"
@@ -71,16 +75,6 @@ __device__ __forceinline__ float block_max(float v, float* scratch) {
   return m;
 }
 
-// Max of v[0, n) (values >= 0) over the calling warp (every lane gets it):
-// lane l takes v[l], v[l + 32], ...; max is exact in any order.
-__device__ __forceinline__ float warp_max_of(const float* __restrict__ v, int n) {
-  float m = 0.f;
-  for (int i = threadIdx.x & 31; i < n; i += 32) m = fmaxf(m, v[i]);
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-  return m;
-}
-
 template <int D>
 __global__ void __launch_bounds__(kPrepThreads)
     prep_pass_a(const uint16_t* __restrict__ k, int64_t n, int rpc, int nchunk,
@@ -121,16 +115,76 @@ __global__ void __launch_bounds__(kPrepThreads)
   }
 }
 
+// Per-head statistics, computed by the last CTA of the head in pass B once
+// every chunk's maxima are written.  Global bound: K_h for every query
+// frame.  Window bound (win.nf > 0; chunk g is frame g): K_a = the largest
+// maximum over the frames query frame a attends, for each a; kmax keeps the
+// head's global maximum; B_h = max_a (scale max_{i in a} ||q_i||) K_a.
+struct HeadOut {
+  float* kq;
+  int nfq;
+  float* kmax;
+  float* bmax;
+  uint8_t* elig;
+};
+
+__device__ void head_finish(int bh, int nchunk, float scale, float tau, const FrameWindow& win,
+                            const float* part_kmax, const float* part_qmax, const HeadOut& o,
+                            float* scratch) {
+  const float* pk = part_kmax + static_cast<size_t>(bh) * nchunk;
+  const float* pq = part_qmax + static_cast<size_t>(bh) * nchunk;
+  // the other CTAs' maxima: read from L2, past any stale L1 line
+  float kg = 0.f, bm = 0.f;
+  if (win.nf == 0) {
+    float qm = 0.f;
+    for (int g = threadIdx.x; g < nchunk; g += kPrepThreads) {
+      kg = fmaxf(kg, __ldcg(pk + g));
+      qm = fmaxf(qm, __ldcg(pq + g));
+    }
+    kg = block_max(kg, scratch);
+    __syncthreads();
+    qm = block_max(qm, scratch);
+    if (threadIdx.x == 0) {
+      scratch[0] = kg;
+      bm = (scale * qm) * kg;
+    }
+    __syncthreads();
+    const float kh = scratch[0];
+    for (int a = threadIdx.x; a < o.nfq; a += kPrepThreads)
+      o.kq[static_cast<size_t>(bh) * o.nfq + a] = kh;
+  } else {
+    for (int a = threadIdx.x; a < nchunk; a += kPrepThreads) {
+      float ka = 0.f;
+      for (int g = 0; g < nchunk; ++g)
+        if (frames_interact(a, g, win.F, win.w, win.R, win.flags)) ka = fmaxf(ka, __ldcg(pk + g));
+      o.kq[static_cast<size_t>(bh) * o.nfq + a] = ka;
+      kg = fmaxf(kg, __ldcg(pk + a));
+      bm = fmaxf(bm, (scale * __ldcg(pq + a)) * ka);
+    }
+    kg = block_max(kg, scratch);
+    __syncthreads();
+    bm = block_max(bm, scratch);
+  }
+  if (threadIdx.x == 0) {
+    const float underflow_limit = 126.0f * 0.693147180559945309f;
+    o.kmax[bh] = kg;
+    o.bmax[bh] = bm;
+    o.elig[bh] = static_cast<uint8_t>(bm <= tau && 2.0f * bm < underflow_limit);
+  }
+}
+
 template <int D>
 __global__ void __launch_bounds__(kPrepThreads)
     prep_pass_b(const uint16_t* __restrict__ q, const uint16_t* __restrict__ k, int64_t n, int rpc,
-                int nchunk, float scale, const float* __restrict__ part_sum, int nsum,
+                int nchunk, float scale, float tau, const float* __restrict__ part_sum, int nsum,
                 float* __restrict__ mu_out, float* __restrict__ qn, float* __restrict__ crow,
-                float* __restrict__ part_kmax, float* __restrict__ part_qmax) {
+                float* __restrict__ part_kmax, float* __restrict__ part_qmax,
+                int* __restrict__ head_count, FrameWindow win, HeadOut ho) {
   constexpr int kLanes = D / 8;
   constexpr int kRows = kPrepThreads / kLanes;
   __shared__ float mu_s[D];
   __shared__ float wmax[kPrepThreads / 32];
+  __shared__ int last;
   ptx::griddep_wait();  // the key sums come from the previous kernel
   const int bh = blockIdx.y, c = blockIdx.x;
   const int lr = threadIdx.x % kLanes, rs = threadIdx.x / kLanes;
@@ -217,97 +271,33 @@ __global__ void __launch_bounds__(kPrepThreads)
   if (threadIdx.x == 0) {
     part_kmax[static_cast<size_t>(bh) * nchunk + c] = kmb;
     part_qmax[static_cast<size_t>(bh) * nchunk + c] = qmb;
-  }
-}
-
-__global__ void __launch_bounds__(kPrepThreads)
-    prep_pass_c(int64_t n, int rpc, int nchunk, float scale, float tau, float* __restrict__ b_rows,
-                float* __restrict__ m_rows, const float* __restrict__ part_kmax,
-                const float* __restrict__ part_qmax, float* __restrict__ kmax,
-                float* __restrict__ bmax, uint8_t* __restrict__ elig) {
-  __shared__ float k_s;
-  ptx::griddep_wait();  // the chunk maxima and row values come from pass B
-  const int bh = blockIdx.y, c = blockIdx.x;
-  if (threadIdx.x < 32) {
-    const float kh = warp_max_of(part_kmax + static_cast<size_t>(bh) * nchunk, nchunk);
-    if (threadIdx.x == 0) k_s = kh;
+    // publish this chunk's maxima, then count it; the head's last chunk
+    // (in whatever order they end) finishes the head
+    __threadfence();
+    last = atomicAdd(head_count + bh, 1) == nchunk - 1;
   }
   __syncthreads();
-  const float kh = k_s;
-  const int64_t r0 = static_cast<int64_t>(c) * rpc;
-  const int64_t r1 = min(n, r0 + rpc);
-  const size_t base = static_cast<size_t>(bh) * n;
-  for (int64_t r = r0 + threadIdx.x; r < r1; r += kPrepThreads) {
-    const float b = (scale * b_rows[base + r]) * kh;  // b_rows holds ||q_i|| here
-    b_rows[base + r] = b;
-    m_rows[base + r] = b + m_rows[base + r];          // m_rows holds c_i here
-  }
-  if (c == 0 && threadIdx.x < 32) {
-    const float qm = warp_max_of(part_qmax + static_cast<size_t>(bh) * nchunk, nchunk);
-    if (threadIdx.x != 0) return;
-    const float bm = (scale * qm) * kh;
-    const float underflow_limit = 126.0f * 0.693147180559945309f;
-    kmax[bh] = kh;
-    bmax[bh] = bm;
-    elig[bh] = static_cast<uint8_t>(bm <= tau && 2.0f * bm < underflow_limit);
-  }
+  if (!last) return;
+  __threadfence();
+  head_finish(bh, nchunk, scale, tau, win, part_kmax, part_qmax, ho, wmax);
+  if (threadIdx.x == 0) head_count[bh] = 0;  // ready for the next launch
 }
 
-// Window bounds (one chunk per frame): K_a = largest per-frame key-norm
-// maximum over the frames query frame a attends; b_i = (scale ||q_i||) K_a;
-// B_h = max_a (scale max_{i in a} ||q_i||) K_a, which equals max_i b_i (the
-// expression is monotone in ||q_i||).  kmax keeps the head's global maximum.
+// b_i and m_i of every row from ||q_i||, c_i and the row's frame bound
+// (in place when the outputs are the inputs).
 __global__ void __launch_bounds__(kPrepThreads)
-    prep_pass_c_window(int64_t n, int rpc, int nchunk, int F, int R, int w, int flags,
-                       float scale, float tau,
-                       float* __restrict__ b_rows, float* __restrict__ m_rows,
-                       const float* __restrict__ part_kmax, const float* __restrict__ part_qmax,
-                       float* __restrict__ kmax, float* __restrict__ bmax,
-                       uint8_t* __restrict__ elig) {
-  __shared__ float k_s;
-  ptx::griddep_wait();  // the chunk maxima and row values come from pass B
-  const int bh = blockIdx.y, a = blockIdx.x;
-  const float* pk = part_kmax + static_cast<size_t>(bh) * nchunk;
-  auto window_max = [&](int f) {
-    float kh = 0.f;
-    for (int g = 0; g < nchunk; ++g)
-      if (frames_interact(f, g, F, w, R, flags)) kh = fmaxf(kh, pk[g]);
-    return kh;
-  };
-  if (threadIdx.x < 32) {  // the warp's lanes take the key frames g = lane, lane + 32, ...
-    float kh = 0.f;
-    for (int g = threadIdx.x; g < nchunk; g += 32)
-      if (frames_interact(a, g, F, w, R, flags)) kh = fmaxf(kh, pk[g]);
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) kh = fmaxf(kh, __shfl_xor_sync(0xffffffffu, kh, o));
-    if (threadIdx.x == 0) k_s = kh;
-  }
-  __syncthreads();
-  const float kh = k_s;
-  const int64_t r0 = static_cast<int64_t>(a) * rpc;
-  const int64_t r1 = min(n, r0 + rpc);
-  const size_t base = static_cast<size_t>(bh) * n;
-  for (int64_t r = r0 + threadIdx.x; r < r1; r += kPrepThreads) {
-    const float b = (scale * b_rows[base + r]) * kh;  // b_rows holds ||q_i|| here
-    b_rows[base + r] = b;
-    m_rows[base + r] = b + m_rows[base + r];          // m_rows holds c_i here
-  }
-  if (a == 0 && threadIdx.x < 32) {  // lanes take the query frames; max is order-free
-    float kg = 0.f, bm = 0.f;
-    for (int f = threadIdx.x; f < nchunk; f += 32) {
-      kg = fmaxf(kg, pk[f]);
-      bm = fmaxf(bm, (scale * part_qmax[static_cast<size_t>(bh) * nchunk + f]) * window_max(f));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) {
-      kg = fmaxf(kg, __shfl_xor_sync(0xffffffffu, kg, o));
-      bm = fmaxf(bm, __shfl_xor_sync(0xffffffffu, bm, o));
-    }
-    if (threadIdx.x != 0) return;
-    const float underflow_limit = 126.0f * 0.693147180559945309f;
-    kmax[bh] = kg;
-    bmax[bh] = bm;
-    elig[bh] = static_cast<uint8_t>(bm <= tau && 2.0f * bm < underflow_limit);
+    prep_finalize_rows(const float* qn, const float* crow, const float* __restrict__ kq, int nfq,
+                       int64_t tq, int64_t n, int64_t total, float scale, float* b_out,
+                       float* m_out) {
+  ptx::griddep_wait();  // the statistics come from pass B
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * kPrepThreads + threadIdx.x; i < total;
+       i += static_cast<int64_t>(gridDim.x) * kPrepThreads) {
+    const int64_t bh = i / n, r = i - bh * n;
+    const float kb = kq[bh * nfq + r / tq];
+    const float b = row_bound(scale, qn[i], kb);
+    const float c = crow[i];
+    b_out[i] = b;
+    m_out[i] = __fadd_rn(b, c);
   }
 }
 
@@ -336,6 +326,8 @@ cudaError_t launch_prepare(const void* q, const void* k, int BH, int64_t N, int 
   // key column sums: pass A's per-chunk sums, or the producer's partial rows
   const float* sums = key_sums ? key_sums : b.part_sum;
   const int nsum = key_sums ? kKeySumRows : b.nchunk;
+  const FrameWindow fw = win ? *win : FrameWindow{0, 0, 0, 0, 0};
+  const HeadOut ho{b.kq, b.nfq, b.kmax, b.bmax, b.elig};
   // every pass may start while its predecessor finishes and waits for it
   // on the device
   cudaError_t e = cudaSuccess;
@@ -345,28 +337,31 @@ cudaError_t launch_prepare(const void* q, const void* k, int BH, int64_t N, int 
                            b.rows_per_chunk, b.nchunk, b.part_sum);
     if (e != cudaSuccess) return e;
     e = launch_dependent(prep_pass_b<128>, grid, dim3(kPrepThreads), 0, stream, q16, k16, N,
-                         b.rows_per_chunk, b.nchunk, scale, sums, nsum, b.mu, b.b_rows, b.m_rows,
-                         b.part_kmax, b.part_qmax);
+                         b.rows_per_chunk, b.nchunk, scale, tau, sums, nsum, b.mu, b.qn_rows,
+                         b.c_rows, b.part_kmax, b.part_qmax, b.head_count, fw, ho);
   } else {
     if (!key_sums)
       e = launch_dependent(prep_pass_a<64>, grid, dim3(kPrepThreads), 0, stream, k16, N,
                            b.rows_per_chunk, b.nchunk, b.part_sum);
     if (e != cudaSuccess) return e;
     e = launch_dependent(prep_pass_b<64>, grid, dim3(kPrepThreads), 0, stream, q16, k16, N,
-                         b.rows_per_chunk, b.nchunk, scale, sums, nsum, b.mu, b.b_rows, b.m_rows,
-                         b.part_kmax, b.part_qmax);
+                         b.rows_per_chunk, b.nchunk, scale, tau, sums, nsum, b.mu, b.qn_rows,
+                         b.c_rows, b.part_kmax, b.part_qmax, b.head_count, fw, ho);
   }
   if (e != cudaSuccess) return e;
-  if (win) {
-    e = launch_dependent(prep_pass_c_window, grid, dim3(kPrepThreads), 0, stream, N,
-                         b.rows_per_chunk, b.nchunk, win->F, win->R, win->w, win->flags, scale,
-                         tau, b.b_rows, b.m_rows, b.part_kmax, b.part_qmax, b.kmax, b.bmax,
-                         b.elig);
-  } else {
-    e = launch_dependent(prep_pass_c, grid, dim3(kPrepThreads), 0, stream, N, b.rows_per_chunk,
-                         b.nchunk, scale, tau, b.b_rows, b.m_rows, b.part_kmax, b.part_qmax,
-                         b.kmax, b.bmax, b.elig);
-  }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_finalize_rows(const PrepBuffers& b, int BH, int64_t N, float scale,
+                                 float* b_out, float* m_out, cudaStream_t stream) {
+  const int64_t total = static_cast<int64_t>(BH) * N;
+  int64_t blocks = (total + kPrepThreads - 1) / kPrepThreads;
+  if (blocks > 4096) blocks = 4096;
+  const cudaError_t e =
+      launch_dependent(prep_finalize_rows, dim3(static_cast<unsigned>(blocks)), dim3(kPrepThreads),
+                       0, stream, static_cast<const float*>(b.qn_rows),
+                       static_cast<const float*>(b.c_rows), static_cast<const float*>(b.kq), b.nfq,
+                       b.tq, N, total, scale, b_out, m_out);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -15,13 +15,15 @@
 //
 // The scratch array, g_prepare_scratch below, holds kStaticSlots chunk slots
 // (a partial key-column sum of up to 128 floats plus two partial maxima per
-// slot): 2048 slots, 1,064,960 bytes.  Every GPU that loads the library holds
-// that memory until the process exits.
+// slot) and, per (b, h), the head's key-norm bound and a counter of finished
+// chunks: 2048 slots, 1,081,344 bytes.  Every GPU that loads the library
+// holds that memory until the process exits.
 //
 // Sharing rules:
 //   - every call uses the same array, and the array keeps whatever the last
-//     call left in it.  Nothing needs to start at zero: each pass writes every
-//     slot that a later pass of the same call reads;
+//     call left in it.  Each pass writes every slot that a later pass of the
+//     same call reads; the counters must start at zero, as they do when the
+//     library is loaded, and every call leaves them at zero again;
 //   - calls whose kernels can overlap on the GPU (for example calls on two
 //     streams of one process with no event ordering them) race on the array
 //     and corrupt each other's results; callers must order such calls.  Each
@@ -38,8 +40,10 @@ namespace {
 
 constexpr int kStaticSlots = 2048;
 constexpr int kStaticMaxDim = 128;
+// part_sum [slots][128], part_kmax [slots], part_qmax [slots], per-head
+// bound [2048], per-head counter [2048] (as int)
 constexpr size_t kStaticFloats =
-    static_cast<size_t>(kStaticSlots) * kStaticMaxDim + 2 * static_cast<size_t>(kStaticSlots);
+    static_cast<size_t>(kStaticSlots) * kStaticMaxDim + 4 * static_cast<size_t>(kStaticSlots);
 
 // Host code must not use this name as a device address: on the host it is a
 // stand-in object.  The device address comes from cudaGetSymbolAddress.
@@ -107,9 +111,11 @@ extern "C" int wsattn_prepare_static(int batch, int heads, int n_tokens, int hea
   // the scratch if the chunking ever asks for more.
   if (static_cast<int64_t>(nchunk) * BH > kStaticSlots) return WSATTN_ERR_BAD_ARG;
 
+  // Pass B leaves ||q_i|| and c_i in the caller's b_rows and m_rows; the
+  // finishing kernel turns them into b_i and m_i in place.
   PrepBuffers b;
-  b.b_rows = b_rows;
-  b.m_rows = m_rows;
+  b.qn_rows = b_rows;
+  b.c_rows = m_rows;
   b.mu = mu;
   b.kmax = kmax;
   b.bmax = bmax;
@@ -117,12 +123,16 @@ extern "C" int wsattn_prepare_static(int batch, int heads, int n_tokens, int hea
   b.part_sum = scratch;
   b.part_kmax = scratch + static_cast<size_t>(kStaticSlots) * kStaticMaxDim;
   b.part_qmax = b.part_kmax + kStaticSlots;
+  b.kq = b.part_qmax + kStaticSlots;  // one bound per (b, h): the head is one frame
+  b.nfq = 1;
+  b.tq = N;
+  b.head_count = reinterpret_cast<int*>(b.kq + kStaticSlots);
   b.nchunk = nchunk;
   b.rows_per_chunk = rpc;
   const float scale = 1.0f / sqrtf(static_cast<float>(head_dim));
-  if (launch_prepare(q, k, BH, N, head_dim, scale, tau, b, nullptr, nullptr,
-                     static_cast<cudaStream_t>(stream)) !=
-      cudaSuccess)
+  const cudaStream_t st = static_cast<cudaStream_t>(stream);
+  if (launch_prepare(q, k, BH, N, head_dim, scale, tau, b, nullptr, nullptr, st) != cudaSuccess ||
+      launch_finalize_rows(b, BH, N, scale, b_rows, m_rows, st) != cudaSuccess)
     return WSATTN_ERR_CUDA;
   return WSATTN_OK;
 }

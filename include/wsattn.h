@@ -210,13 +210,15 @@ int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, 
  *   kmax, bmax        fp32 [batch*heads] outputs: K_h and B_h
  *   elig              uint8 [batch*heads] output
  * Its scratch is one fixed array in the library's device image: 2048 chunk
- * slots (1,064,960 bytes), held by every GPU that loads the library until
- * the process exits.  batch*heads above 2048 is rejected with BAD_ARG before
- * anything is enqueued (so is a row chunking that would need more than the
- * 2048 slots, which cannot happen on a GPU with fewer than 683 SMs).  All calls share the array and it keeps the last
- * call's contents; nothing in it needs to start at zero.  Calls whose
- * kernels can overlap on the GPU race on it and must be ordered by the
- * caller.  The first call on a device looks up the array's device address
+ * slots and 2048 per-head entries (1,081,344 bytes), held by every GPU that
+ * loads the library until the process exits.  batch*heads above 2048 is
+ * rejected with BAD_ARG before anything is enqueued (so is a row chunking
+ * that would need more than the 2048 slots, which cannot happen on a GPU
+ * with fewer than 683 SMs).  All calls share the array and it keeps the last
+ * call's contents; the only part that must start at zero, the per-head
+ * counters of finished chunks, is zero when the library loads and every
+ * call leaves it at zero.  Calls whose kernels can overlap on the GPU race
+ * on it and must be ordered by the caller.  The first call on a device looks up the array's device address
  * with that device current (so make it before any stream capture).
  * Errors: BAD_ARG, UNSUPPORTED (head_dim), CUDA.
  */
