@@ -587,7 +587,8 @@ def main():
     ap.add_argument("--cpu-budget", type=float, default=12.0,
                     help="seconds of oracle time for the cpu_baseline sample")
     ap.add_argument("--other-configs", default="sr_long,dense,small,tiny",
-                    help="comma-separated workloads timed after the main one (rank 0, N=1 only)")
+                    help="comma-separated workloads timed after the main one (rank 0, N=1 "
+                         "only); 'none' or '' for none")
     args = ap.parse_args()
     from workloads import WORKLOADS
     wl = WORKLOADS[args.workload]
@@ -596,7 +597,8 @@ def main():
         run_reference(args, wl, world, rank)
         return
     line = run_gpu(args, wl, world, rank, local)
-    if rank == 0 and line is not None and world == 1 and args.other_configs:
+    if (rank == 0 and line is not None and world == 1 and args.other_configs
+            and args.other_configs != "none"):
         steps_of = {"sr_long": 30, "dense": 30, "sr": 60, "small": 200, "tiny": 200}
         line["configs"] = {}
         for name in [x for x in args.other_configs.split(",") if x and x != wl.name]:

@@ -156,9 +156,8 @@ int ensure_workspace(wsattn_plan_s* p, int batch, cudaStream_t stream) {
   const int BH = batch * hp.H;
   int nchunk = 0, rpc = 0;
   wsattn::prepare_chunking(BH, hp.N, p->num_sms, &nchunk, &rpc);
-  // Chunk slots: any batch <= this one needs at most BH * max(1, 3 SMs / BH)
-  // <= 3 SMs + BH of them (prepare_chunking fills one wave); 4 SMs + BH
-  // leaves room to spare.
+  // Chunk slots: any batch <= this one needs at most BH * max(1, 4 SMs / BH)
+  // <= 4 SMs + BH of them (prepare_chunking fills one wave).
   size_t slots = static_cast<size_t>(BH) * nchunk;
   const size_t bound = static_cast<size_t>(4) * p->num_sms + BH;
   if (slots < bound) slots = bound;

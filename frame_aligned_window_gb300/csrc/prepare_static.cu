@@ -106,9 +106,9 @@ extern "C" int wsattn_prepare_static(int batch, int heads, int n_tokens, int hea
 
   int nchunk = 0, rpc = 0;
   prepare_chunking(BH, N, num_sms, &nchunk, &rpc);
-  // prepare_chunking gives at most max(BH, 3 * SMs) chunks in all, so this
-  // holds on every GPU with fewer than 683 SMs; refuse rather than overrun
-  // the scratch if the chunking ever asks for more.
+  // prepare_chunking gives at most max(BH, 4 * SMs) chunks in all, so this
+  // holds on every GPU with at most 512 SMs; refuse rather than overrun the
+  // scratch if the chunking ever asks for more.
   if (static_cast<int64_t>(nchunk) * BH > kStaticSlots) return WSATTN_ERR_BAD_ARG;
 
   // Pass B leaves ||q_i|| and c_i in the caller's b_rows and m_rows; the

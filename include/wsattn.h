@@ -214,7 +214,7 @@ int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, 
  * loads the library until the process exits.  batch*heads above 2048 is
  * rejected with BAD_ARG before anything is enqueued (so is a row chunking
  * that would need more than the 2048 slots, which cannot happen on a GPU
- * with fewer than 683 SMs).  All calls share the array and it keeps the last
+ * with at most 512 SMs).  All calls share the array and it keeps the last
  * call's contents; the only part that must start at zero, the per-head
  * counters of finished chunks, is zero when the library loads and every
  * call leaves it at zero.  Calls whose kernels can overlap on the GPU race
