@@ -46,10 +46,12 @@
 // lists, longest first) and head by head inside a class, so the CTAs running
 // at one time stream the same head's keys and values through L2.  They are
 // dealt out on the device: a CTA's TMA warp takes the next index from a
-// global counter when it starts on an item and passes it to the CTA's other
-// roles through a small queue in shared memory, so the items go to whichever
-// CTA is free first (list scheduling in the longest-first order) and the
-// deal adapts to the actual cost of each item (online heads are slower).
+// global counter two key steps before it has loaded the current item's last
+// keys, decodes it (tile, b*h and the tile's record) and passes it to the
+// CTA's other roles through a small queue in shared memory, so the items go
+// to whichever CTA is free first (list scheduling in the longest-first order)
+// and the deal adapts to the actual cost of each item (online heads are
+// slower).  The next item's Q tile is loaded while the current one runs.
 // The last CTA to finish resets the counter.  The kernel is a dependent
 // launch: its prologue overlaps the end of the statistics pass before it.
 //
@@ -80,6 +82,9 @@ constexpr uint32_t kTmemCols = 512;
 // from a global counter and passes it to the CTA's other roles through a
 // small queue in shared memory.
 constexpr int kItemQueue = 4;
+// A queue slot: the item index (-1: none left), its tile and b*h, and the
+// tile's record, decoded once by the TMA warp.
+constexpr int kQWords = 4 + static_cast<int>(sizeof(WorkTile) / 4);
 constexpr uint32_t kItemReaders = 3 + kSoftmaxWarps;  // V producer, both issuers, every softmax warp
 
 // mbarrier slots
@@ -116,7 +121,7 @@ struct Shared {
   uint32_t q, k, v, bars;  // shared-window addresses
   uint32_t ostage;         // epilogue staging chunks (kOChunkBytes per softmax warp)
   float* xch_m;            // [2][kNumWG][128]
-  volatile int32_t* iq;    // [kItemQueue] work items (-1: no more)
+  volatile int32_t* iq;    // [kItemQueue][kQWords] decoded work items
   float* xch_l;            // [2][kNumWG][128]
   volatile int* abort_flag;
   int* status;
@@ -173,24 +178,66 @@ __device__ __forceinline__ void warp_arrive(uint32_t b) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(b);
 }
 
-// TMA warp: takes the next work item from the launch's counter and posts it
-// to the queue.  Returns the item, -1 once none is left (posted too, so the
-// other roles stop), -2 on an expired wait.
+struct Item {
+  int tile, bh;
+};
+
+// Work item -> (tile, b*h): classes in order, heads in order inside a class.
+__device__ __forceinline__ Item map_item(const FwdParams& p, int it) {
+  int c = 0;
+  while (c + 1 < p.n_cls && it >= p.bh * __ldg(p.cls + c + 1)) ++c;
+  const int beg = __ldg(p.cls + c);
+  const int n = __ldg(p.cls + c + 1) - beg;
+  const int o = it - p.bh * beg;
+  return Item{beg + o % n, o / n};
+}
+
+// TMA warp: takes the next work item from the launch's counter, decodes it
+// and posts it to the queue.  Returns the item, -1 once none is left (posted
+// too, so the other roles stop), -2 on an expired wait.
 __device__ __forceinline__ int post_item(const FwdParams& p, const Shared& s, ItemPos& q,
-                                         int n_items) {
+                                         int n_items, Item& im, WorkTile& t) {
   if (!wait(s, bar(s, B_IQEMPTY0 + q.slot), q.phase ^ 1u, kStatusTimeoutProducer)) return -2;
   int it = atomicAdd(p.work, 1);
   if (it >= n_items) it = -1;
-  s.iq[q.slot] = it;
+  volatile int32_t* e = s.iq + q.slot * kQWords;
+  if (it >= 0) {
+    im = map_item(p, it);
+    if (!WSATTN_BOUNDS(p.status, im.tile >= 0 && im.tile < p.n_tiles && im.bh >= 0 &&
+                                     im.bh < p.bh))
+      im = Item{0, 0};
+    t = p.tiles[im.tile];
+    e[1] = im.tile;
+    e[2] = im.bh;
+    const int32_t* tw = reinterpret_cast<const int32_t*>(&t);
+#pragma unroll
+    for (int i = 0; i < static_cast<int>(sizeof(WorkTile) / 4); ++i) e[4 + i] = tw[i];
+  }
+  e[0] = it;
   mbar_arrive(bar(s, B_IQFULL0 + q.slot));
   q.next();
   return it;
 }
 
+// The decoded item of a queue slot.
+__device__ __forceinline__ int slot_item(const Shared& s, uint32_t slot, Item& im, WorkTile& t) {
+  const volatile int32_t* e = s.iq + slot * kQWords;
+  const int it = e[0];
+  if (it >= 0) {
+    im.tile = e[1];
+    im.bh = e[2];
+    int32_t* tw = reinterpret_cast<int32_t*>(&t);
+#pragma unroll
+    for (int i = 0; i < static_cast<int>(sizeof(WorkTile) / 4); ++i) tw[i] = e[4 + i];
+  }
+  return it;
+}
+
 // An issuer thread's next work item (-1: none left, -2: expired wait).
-__device__ __forceinline__ int read_item(const Shared& s, ItemPos& q, int code) {
+__device__ __forceinline__ int read_item(const Shared& s, ItemPos& q, int code, Item& im,
+                                         WorkTile& t) {
   if (!wait(s, bar(s, B_IQFULL0 + q.slot), q.phase, code)) return -2;
-  const int it = s.iq[q.slot];
+  const int it = slot_item(s, q.slot, im, t);
   mbar_arrive(bar(s, B_IQEMPTY0 + q.slot));
   q.next();
   return it;
@@ -203,9 +250,10 @@ __device__ __forceinline__ bool wait_issuer(const Shared& s, uint32_t b, uint32_
 }
 
 // An issuer warp's next work item: every lane waits and reads, one arrives.
-__device__ __forceinline__ int read_item_issuer(const Shared& s, ItemPos& q) {
+__device__ __forceinline__ int read_item_issuer(const Shared& s, ItemPos& q, Item& im,
+                                                WorkTile& t) {
   if (!wait_issuer(s, bar(s, B_IQFULL0 + q.slot), q.phase)) return -2;
-  const int it = s.iq[q.slot];
+  const int it = slot_item(s, q.slot, im, t);
   __syncwarp();
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar(s, B_IQEMPTY0 + q.slot));
   q.next();
@@ -213,9 +261,10 @@ __device__ __forceinline__ int read_item_issuer(const Shared& s, ItemPos& q) {
 }
 
 // A softmax warp's next work item (warp-uniform; one arrival per warp).
-__device__ __forceinline__ int read_item_warp(const Shared& s, ItemPos& q) {
+__device__ __forceinline__ int read_item_warp(const Shared& s, ItemPos& q, Item& im,
+                                             WorkTile& t) {
   if (!wait_warp(s, bar(s, B_IQFULL0 + q.slot), q.phase)) return -2;
-  const int it = s.iq[q.slot];
+  const int it = slot_item(s, q.slot, im, t);
   warp_arrive(bar(s, B_IQEMPTY0 + q.slot));
   q.next();
   return it;
@@ -253,20 +302,6 @@ __device__ __forceinline__ TmemCols tmem_cols(int step_keys) {
   const uint32_t st = static_cast<uint32_t>(step_keys);
   return TmemCols{0u, static_cast<uint32_t>(D), static_cast<uint32_t>(D) + st, st / 2u,
                   static_cast<uint32_t>(D) + 2u * st};
-}
-
-struct Item {
-  int tile, bh;
-};
-
-// Work item -> (tile, b*h): classes in order, heads in order inside a class.
-__device__ __forceinline__ Item map_item(const FwdParams& p, int it) {
-  int c = 0;
-  while (c + 1 < p.n_cls && it >= p.bh * __ldg(p.cls + c + 1)) ++c;
-  const int beg = __ldg(p.cls + c);
-  const int n = __ldg(p.cls + c + 1) - beg;
-  const int o = it - p.bh * beg;
-  return Item{beg + o % n, o / n};
 }
 
 // Position in a ring of `n` stages: slot and the parity of its current use.
@@ -346,29 +381,55 @@ __device__ void producer_qk(const FwdParams& p, const Shared& s) {
   };
   const int n_items = p.n_tiles * p.bh;
   ItemPos iq;
-  while (true) {
-    const int it = post_item(p, s, iq, n_items);
-    if (it == -2) return drain();
-    if (it < 0) break;
-    const Item im = map_item(p, it);
-    if (!WSATTN_BOUNDS(p.status, im.tile >= 0 && im.tile < p.n_tiles && im.bh >= 0 &&
-                                     im.bh < p.bh))
-      return;
-    const WorkTile t = p.tiles[im.tile];
-    const int y0 = im.bh * p.n;
-    [[maybe_unused]] const int rows = p.bh * p.n;
-    if (!wait(s, bar(s, B_QEMPTY), (qc & 1u) ^ 1u, kStatusTimeoutProducer)) return drain();
+  [[maybe_unused]] const int rows = p.bh * p.n;
+  // Takes the next item from the counter; false on an expired wait.
+  auto take = [&](int& it, Item& im, WorkTile& t) {
+    it = post_item(p, s, iq, n_items, im, t);
+    return it != -2;
+  };
+  auto load_qtile = [&](const Item& im, const WorkTile& t) {
     mbar_arrive_expect_tx(bar(s, B_QFULL), kTileM * D * 2);
     if (WSATTN_BOUNDS(p.status, t.row0 >= 0 && t.nvalid > 0 && t.nvalid <= kTileM &&
                                     t.row0 + t.nvalid <= p.n)) {
 #pragma unroll
       for (int c = 0; c < kBoxes; ++c)
-        tma_load_2d(s.q + c * (kTileM * 128), &p.tm_q, bar(s, B_QFULL), c * 64, y0 + t.row0);
+        tma_load_2d(s.q + c * (kTileM * 128), &p.tm_q, bar(s, B_QFULL), c * 64,
+                    im.bh * p.n + t.row0);
     }
     ++qc;
+  };
+  // The next item is taken kLookahead K steps before the current item's last
+  // one, and its Q tile is loaded as soon as the staging buffer is free
+  // (tested without blocking, so the K loads never wait for it): the Q tile
+  // is then resident when the softmax warps finish the current item.
+  constexpr int kLookahead = 2;
+  int it;
+  Item im{};
+  WorkTile t{};
+  if (!take(it, im, t)) return drain();
+  bool q_pending = it >= 0;
+  while (it >= 0) {
+    const int y0 = im.bh * p.n;
+    if (q_pending) {
+      if (!wait(s, bar(s, B_QEMPTY), (qc & 1u) ^ 1u, kStatusTimeoutProducer)) return drain();
+      load_qtile(im, t);
+    }
+    int nxt = -1;
+    Item nim{};
+    WorkTile nt{};
+    bool nq_pending = false;
+    const int post_at = t.nstep > kLookahead ? t.nstep - kLookahead : 0;
     Steps ks;
     ks.init(t);
     for (int j = 0; j < t.nstep; ++j) {
+      if (j == post_at) {
+        if (!take(nxt, nim, nt)) return drain();
+        nq_pending = nxt >= 0;
+      }
+      if (nq_pending && mbar_test_wait(bar(s, B_QEMPTY), (qc & 1u) ^ 1u)) {
+        load_qtile(nim, nt);
+        nq_pending = false;
+      }
       int nb;
       const int row = y0 + ks.next(G, nb) * bk;
       if (!wait(s, bar(s, B_KEMPTY0 + kr.slot), kr.phase ^ 1u, kStatusTimeoutProducer))
@@ -387,6 +448,10 @@ __device__ void producer_qk(const FwdParams& p, const Shared& s) {
       kiss |= 1u << kr.slot;
       kr.next(nk);
     }
+    it = nxt;
+    im = nim;
+    t = nt;
+    q_pending = nq_pending;
   }
 }
 
@@ -403,14 +468,11 @@ __device__ void producer_v(const FwdParams& p, const Shared& s) {
   auto drain = [&]() { drain_loads(bar(s, B_VFULL0), static_cast<int>(nv), vph, viss); };
   ItemPos iq;
   while (true) {
-    const int it = read_item(s, iq, kStatusTimeoutProducer);
+    Item im;
+    WorkTile t;
+    const int it = read_item(s, iq, kStatusTimeoutProducer, im, t);
     if (it == -2) return drain();
     if (it < 0) break;
-    const Item im = map_item(p, it);
-    if (!WSATTN_BOUNDS(p.status, im.tile >= 0 && im.tile < p.n_tiles && im.bh >= 0 &&
-                                     im.bh < p.bh))
-      return;
-    const WorkTile t = p.tiles[im.tile];
     const int y0 = im.bh * p.n;
     Steps vs;
     vs.init(t);
@@ -464,10 +526,9 @@ __device__ void qk_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
   Steps qs;
   ItemPos iq;
   while (true) {
-    const int it = read_item_issuer(s, iq);
-    if (it < 0) break;
-    const Item im = map_item(p, it);
-    const WorkTile t = p.tiles[im.tile];
+    Item im;
+    WorkTile t;
+    if (read_item_issuer(s, iq, im, t) < 0) break;
     qs.init(t);
     if (!wait_issuer(s, bar(s, B_QTFULL), tiles_done & 1u)) return;
     tc_fence_after();
@@ -520,10 +581,9 @@ __device__ void pv_issuer(const FwdParams& p, const Shared& s, uint32_t tbase) {
   Steps ps;
   ItemPos iq;
   while (true) {
-    const int it = read_item_issuer(s, iq);
-    if (it < 0) break;
-    const Item im = map_item(p, it);
-    const WorkTile t = p.tiles[im.tile];
+    Item im;
+    WorkTile t;
+    if (read_item_issuer(s, iq, im, t) < 0) break;
     const int nstep = t.nstep;
     ps.init(t);
     for (int j = 0; j < nstep; ++j) {
@@ -638,6 +698,38 @@ __device__ __forceinline__ void exp_chunks(const uint32_t (&sv)[MAXC][16], int n
   }
 }
 
+// A softmax thread's view of a work item: the tile, its path, and the
+// statistics behind its own row's fixed max.  Formed for the next item before
+// the current item's epilogue, so that the global loads of the row and frame
+// statistics complete while the epilogue runs rather than in front of the
+// next item's first key step.
+struct RowItem {
+  Item im;
+  WorkTile t;
+  size_t grow;
+  float qn, kq, c;  // ||q_i||, the frame's key-norm bound, c_i (0 for rows past the frame)
+  bool online, valid;
+  // -m_i in log2 units: the row's fixed max m_i = b_i + c_i, b_i = (scale ||q_i||) K
+  __device__ __forceinline__ float nb_fixed(float scale) const {
+    return valid ? -__fadd_rn(row_bound(scale, qn, kq), c) * kLog2e : 0.f;
+  }
+};
+
+__device__ __forceinline__ RowItem row_item(const FwdParams& p, const Item& im,
+                                            const WorkTile& t, int r) {
+  RowItem x;
+  x.im = im;
+  x.t = t;
+  x.online = p.force_path >= 0 ? (p.force_path == 1) : (p.elig[x.im.bh] == 0);
+  x.grow = static_cast<size_t>(x.im.bh) * p.n + x.t.row0 + r;
+  x.valid = r < x.t.nvalid && WSATTN_BOUNDS(p.status, x.grow < static_cast<size_t>(p.bh) * p.n);
+  // loads only: their values are first used when the item starts
+  x.qn = x.valid ? p.qn_rows[x.grow] : 0.f;
+  x.kq = x.valid ? p.kq[static_cast<size_t>(x.im.bh) * p.nfq + x.t.row0 / p.tq] : 0.f;
+  x.c = x.valid ? p.c_rows[x.grow] : 0.f;
+  return x;
+}
+
 template <int D, int MAXC>
 __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) {
   const int warp = threadIdx.x / 32;
@@ -661,27 +753,22 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
   Ring pr;          // P buffer
 
   ItemPos iq;
-  int it = read_item_warp(s, iq);
-  if (it < 0) return;
-  if (!load_q<D>(s, lane + tc_.q, wg, r, p.tiles[map_item(p, it).tile].nvalid, qc)) return;
+  Item im0;
+  WorkTile t0;
+  if (read_item_warp(s, iq, im0, t0) < 0) return;
+  RowItem cur = row_item(p, im0, t0, r);
+  if (!load_q<D>(s, lane + tc_.q, wg, r, cur.t.nvalid, qc)) return;
   while (true) {
-    const Item im = map_item(p, it);
-    const WorkTile t = p.tiles[im.tile];
-    const bool online = p.force_path >= 0 ? (p.force_path == 1) : (p.elig[im.bh] == 0);
-    const size_t grow = static_cast<size_t>(im.bh) * p.n + t.row0 + r;
-    const bool valid =
-        r < t.nvalid && WSATTN_BOUNDS(p.status, grow < static_cast<size_t>(p.bh) * p.n);
+    const Item im = cur.im;
+    const WorkTile t = cur.t;
+    const bool online = cur.online;
+    const size_t grow = cur.grow;
+    const bool valid = cur.valid;
+    const float nb_fixed = cur.nb_fixed(p.scale);
     Steps st;
     st.init(t);
     float l = 0.f;
     float m = -INFINITY;
-    // the row's fixed max m_i = b_i + c_i, b_i = (scale ||q_i||) K of its frame
-    const float nb_fixed =
-        valid ? -__fadd_rn(row_bound(p.scale, p.qn_rows[grow],
-                                     p.kq[static_cast<size_t>(im.bh) * p.nfq + t.row0 / p.tq]),
-                           p.c_rows[grow]) *
-                    kLog2e
-              : 0.f;
     if (!online) {
       // Fixed max: every step is load, exp, pack, store; the row sum
       // accumulates.
@@ -809,12 +896,17 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
       }
     }
 
-    // Stage the next tile's Q so its first QK products overlap this epilogue.
-    const int nxt = read_item_warp(s, iq);
+    // Stage the next tile's Q so its first QK products overlap this epilogue,
+    // and start the loads of its row parameters.
+    Item nim;
+    WorkTile ntl;
+    const int nxt = read_item_warp(s, iq, nim, ntl);
     if (nxt == -2) return;
-    if (nxt >= 0 &&
-        !load_q<D>(s, lane + tc_.q, wg, r, p.tiles[map_item(p, nxt).tile].nvalid, qc))
-      return;
+    RowItem nx;
+    if (nxt >= 0) {
+      nx = row_item(p, nim, ntl, r);
+      if (!load_q<D>(s, lane + tc_.q, wg, r, nx.t.nvalid, qc)) return;
+    }
 
     if (!wait_warp(s, bar(s, B_OFULL), tiles_done & 1u)) return;
     // the row sum is the sum of the warpgroups' partial sums (fixed order)
@@ -876,7 +968,7 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
       }
     }
     if (nxt < 0) break;
-    it = nxt;
+    cur = nx;
   }
 }
 
@@ -897,7 +989,7 @@ __global__ void __launch_bounds__(kThreads, 1) wsattn_fwd_kernel(const __grid_co
   s.xch_m = reinterpret_cast<float*>(gbars + 8 * B_COUNT + 16);
   s.xch_l = s.xch_m + 2 * kNumWG * kTileM;
   s.iq = reinterpret_cast<volatile int32_t*>(s.xch_l + 2 * kNumWG * kTileM);
-  s.ostage = (s.bars + 8u * B_COUNT + 16u + kXchBytes + 4u * kItemQueue + 511u) & ~511u;
+  s.ostage = (s.bars + 8u * B_COUNT + 16u + kXchBytes + 4u * kQWords * kItemQueue + 511u) & ~511u;
   uint32_t* tslot = reinterpret_cast<uint32_t*>(gbars + 8 * B_COUNT);
   s.abort_flag = reinterpret_cast<volatile int*>(tslot + 1);
   s.status = p.status;
@@ -1044,7 +1136,7 @@ cudaError_t launch_d(const FwdParams& p, int grid, size_t smem, cudaStream_t str
 size_t forward_smem_bytes(int D, int step_keys, int stages_k, int stages_v) {
   const size_t stage = static_cast<size_t>(step_keys) * D * 2;
   return 1024 + static_cast<size_t>(kTileM) * D * 2 + (stages_k + stages_v) * stage +
-         8 * B_COUNT + 16 + kXchBytes + 4 * kItemQueue + 512 + kOStageBytes;
+         8 * B_COUNT + 16 + kXchBytes + 4 * kQWords * kItemQueue + 512 + kOStageBytes;
 }
 
 void forward_stages(int D, int step_keys, size_t smem_optin, int* stages_k, int* stages_v) {
