@@ -179,6 +179,10 @@ def test_block_sizes_step_buffers(bk):
     (53, 2, 3, 64, 3, 2, 160, 1),      # two reference frames, D=64, batch 2
     (54, 1, 1, 128, 6, 1, 256, 10),    # window beyond the frame count (dense)
     (55, 1, 2, 128, 3, 1, 144, 1),     # T = 128 + 16: a full tile and a 16-row tail
+    # one-step tiles, about ten work items per CTA: the next item is taken
+    # at the first key step and the item queue wraps many times
+    (57, 1, 8, 128, 200, 0, 16, 0),
+    (58, 1, 4, 128, 60, 1, 80, 1),     # two-step tiles, 240 work items
 ])
 def test_edge_shapes_full_parity(case):
     seed, B, H, D, F, R, T, w = case
