@@ -10,7 +10,7 @@ instead (the tests use it for the bounds-checking libwsattn_debug.so).
 
 The names mirror the C ABI:
     wsattn_plan, wsattn_plan_ex, wsattn_plan_destroy, wsattn_prepare, wsattn_forward,
-    wsattn_plan_info, wsattn_get_block_map, wsattn_get_csr, wsattn_get_stats,
+    wsattn_plan_info, wsattn_get_tiles, wsattn_get_block_map, wsattn_get_csr, wsattn_get_stats,
     wsattn_plan_set_debug, wsattn_plan_set_bound, wsattn_device_status,
     wsattn_selftest_timeout, wsattn_status_string, wsattn_prepare_static, wsattn_produce,
     wsattn_build_flags
@@ -29,7 +29,8 @@ DEBUG_LIB_PATH = os.path.join(_HERE, "libwsattn_debug.so")
 # C ABI entry points declared in include/wsattn.h
 EXPORTS = (
     "wsattn_plan", "wsattn_plan_ex", "wsattn_plan_destroy", "wsattn_prepare", "wsattn_forward",
-    "wsattn_plan_info", "wsattn_get_block_map", "wsattn_get_csr", "wsattn_get_stats",
+    "wsattn_plan_info", "wsattn_get_tiles", "wsattn_get_block_map", "wsattn_get_csr",
+    "wsattn_get_stats",
     "wsattn_plan_set_debug", "wsattn_plan_set_bound", "wsattn_device_status",
     "wsattn_selftest_timeout", "wsattn_status_string", "wsattn_prepare_static",
     "wsattn_produce", "wsattn_build_flags",
@@ -72,6 +73,7 @@ _lib.wsattn_forward.argtypes = [_P, _I, _P, _P, _P, _P, _P]
 _lib.wsattn_plan_info.argtypes = [_P, _P, _I]
 _lib.wsattn_get_block_map.argtypes = [_P, _P, _SZ]
 _lib.wsattn_get_csr.argtypes = [_P, _P, _P, _SZ, _SZ]
+_lib.wsattn_get_tiles.argtypes = [_P, _P, _SZ, _P, _SZ]
 _lib.wsattn_get_stats.argtypes = [_P, _P, _P, _P, _P, _P, _P, _P]
 _lib.wsattn_plan_set_debug.argtypes = [_P, _I, _F]
 _lib.wsattn_plan_set_bound.argtypes = [_P, _I]
@@ -257,6 +259,20 @@ def wsattn_get_block_map(plan: Plan) -> np.ndarray:
     _check(_lib.wsattn_get_block_map(plan.handle, out.ctypes.data, out.size),
            "wsattn_get_block_map")
     return out
+
+
+def wsattn_get_tiles(plan: Plan):
+    """The forward work list: int32 [tiles, 10] {row0, nvalid, nblk, run0, len0,
+    run1, nstep, kbeg, gsz, gtab} and the merged tails' group table int32
+    [groups, 4] {run0, len0, run1, len1}."""
+    tiles = np.zeros((plan.tiles_per_head, 10), dtype=np.int32)
+    # each merged tile holds at most 8 row groups (tails of at least 16 rows)
+    groups = np.zeros((8 * plan.tiles_per_head, 4), dtype=np.int32)
+    _check(_lib.wsattn_get_tiles(plan.handle, tiles.ctypes.data, tiles.size, groups.ctypes.data,
+                                 groups.size), "wsattn_get_tiles")
+    merged = tiles[:, 8] > 0
+    n_groups = int((tiles[merged, 1] // tiles[merged, 8]).sum())  # nvalid = groups x gsz
+    return tiles, groups[:n_groups]
 
 
 def wsattn_get_csr(plan: Plan):

@@ -3,6 +3,7 @@
 // host beyond argument checks and the block map (plan.cpp).
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstring>
 #include <mutex>
@@ -23,6 +24,7 @@ struct wsattn_plan_s {
   size_t smem_optin = 0;
   int clock_khz = 0;
   WorkTile* d_tiles = nullptr;
+  int32_t* d_grp = nullptr;  // group table of the merged tail tiles (at least one entry)
   int32_t* d_cls = nullptr;
   int* d_status = nullptr;
   int* d_work = nullptr;  // the forward's work counters (zero between launches)
@@ -131,7 +133,10 @@ int ensure_device(wsattn_plan_s* p) {
   const HostPlan& hp = p->hp;
   const size_t tiles_bytes = hp.tiles.size() * sizeof(WorkTile);
   const size_t cls_bytes = hp.cls.size() * sizeof(int32_t);
+  const size_t grp_bytes =
+      std::max<size_t>(hp.grp.size(), wsattn::kGroupInts) * sizeof(int32_t);
   if (cudaMalloc(&p->d_tiles, tiles_bytes) != cudaSuccess ||
+      cudaMalloc(&p->d_grp, grp_bytes) != cudaSuccess ||
       cudaMalloc(&p->d_cls, cls_bytes) != cudaSuccess ||
       cudaMalloc(&p->d_status, sizeof(int)) != cudaSuccess ||
       cudaMalloc(&p->d_work, 2 * sizeof(int)) != cudaSuccess)
@@ -139,6 +144,9 @@ int ensure_device(wsattn_plan_s* p) {
   if (cudaMemcpy(p->d_tiles, hp.tiles.data(), tiles_bytes, cudaMemcpyHostToDevice) !=
           cudaSuccess ||
       cudaMemcpy(p->d_cls, hp.cls.data(), cls_bytes, cudaMemcpyHostToDevice) != cudaSuccess ||
+      cudaMemset(p->d_grp, 0, grp_bytes) != cudaSuccess ||
+      (!hp.grp.empty() && cudaMemcpy(p->d_grp, hp.grp.data(), hp.grp.size() * sizeof(int32_t),
+                                     cudaMemcpyHostToDevice) != cudaSuccess) ||
       cudaMemset(p->d_status, 0, sizeof(int)) != cudaSuccess ||
       cudaMemset(p->d_work, 0, 2 * sizeof(int)) != cudaSuccess)
     return WSATTN_ERR_CUDA;
@@ -241,11 +249,13 @@ void free_device(wsattn_plan_s* p) {
   if (p->prod_ws) cudaFree(p->prod_ws);
   p->prod_ws = nullptr;
   if (p->d_tiles) cudaFree(p->d_tiles);
+  if (p->d_grp) cudaFree(p->d_grp);
   if (p->d_cls) cudaFree(p->d_cls);
   if (p->d_status) cudaFree(p->d_status);
   if (p->d_work) cudaFree(p->d_work);
   if (p->ws) cudaFree(p->ws);
   p->d_tiles = nullptr;
+  p->d_grp = nullptr;
   p->d_cls = nullptr;
   p->d_status = nullptr;
   p->d_work = nullptr;
@@ -401,11 +411,13 @@ int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, 
   // rows: K and V are loaded one box of a whole step per 64-column slab.
   const int step_keys = hp.G * hp.bk;
   if (!encode_map(&prm.tm_q, q, rows, hp.D, wsattn::kTileM) ||
+      (hp.gsz > 0 && !encode_map(&prm.tm_qg, q, rows, hp.D, hp.gsz)) ||
       !encode_map(&prm.tm_k, k, rows, hp.D, step_keys) ||
       !encode_map(&prm.tm_v, v, rows, hp.D, step_keys) ||
       !encode_out_map(&prm.tm_o, out, rows, hp.D))
     return WSATTN_ERR_CUDA;
   prm.tiles = plan->d_tiles;
+  prm.grp = plan->d_grp;
   prm.cls = plan->d_cls;
   prm.n_cls = static_cast<int>(hp.cls.size()) - 1;
   prm.qn_rows = plan->buf.qn_rows;
@@ -451,6 +463,19 @@ int wsattn_plan_info(wsattn_plan_t plan, int64_t* info, int n) {
                          hp.H,
                          hp.active_pairs};
   for (int i = 0; i < n && i < 10; ++i) info[i] = v[i];
+  return WSATTN_OK;
+}
+
+int wsattn_get_tiles(wsattn_plan_t plan, int32_t* tiles, size_t n_tiles, int32_t* groups,
+                     size_t n_groups) {
+  if (!plan) return WSATTN_ERR_BAD_ARG;
+  const HostPlan& hp = plan->hp;
+  constexpr size_t kTileInts = sizeof(WorkTile) / sizeof(int32_t);
+  if ((!tiles && !hp.tiles.empty()) || n_tiles < hp.tiles.size() * kTileInts ||
+      (!groups && !hp.grp.empty()) || n_groups < hp.grp.size())
+    return WSATTN_ERR_BAD_ARG;
+  if (!hp.tiles.empty()) std::memcpy(tiles, hp.tiles.data(), hp.tiles.size() * sizeof(WorkTile));
+  if (!hp.grp.empty()) std::memcpy(groups, hp.grp.data(), hp.grp.size() * sizeof(int32_t));
   return WSATTN_OK;
 }
 

@@ -61,6 +61,8 @@
 // released on the way out.
 #include <cuda_bf16.h>
 
+#include <type_traits>
+
 #include "internal.h"
 #include "ptx.cuh"
 
@@ -387,14 +389,29 @@ __device__ void producer_qk(const FwdParams& p, const Shared& s) {
     it = post_item(p, s, iq, n_items, im, t);
     return it != -2;
   };
+  // A merged tail tile's Q comes one row group at a time (gsz rows from
+  // token row0 + i*T into tile rows i*gsz onwards; gsz*128 bytes is a
+  // multiple of 1024, so every box starts on the swizzle's period).
   auto load_qtile = [&](const Item& im, const WorkTile& t) {
-    mbar_arrive_expect_tx(bar(s, B_QFULL), kTileM * D * 2);
+    const int ng = t.gsz ? t.nvalid / t.gsz : 0;
+    mbar_arrive_expect_tx(bar(s, B_QFULL), (t.gsz ? t.nvalid : kTileM) * D * 2);
     if (WSATTN_BOUNDS(p.status, t.row0 >= 0 && t.nvalid > 0 && t.nvalid <= kTileM &&
-                                    t.row0 + t.nvalid <= p.n)) {
+                                    (t.gsz ? t.nvalid % t.gsz == 0 &&
+                                                 t.row0 + (ng - 1) * p.tq + t.gsz <= p.n
+                                           : t.row0 + t.nvalid <= p.n))) {
+      if (t.gsz == 0) {
 #pragma unroll
-      for (int c = 0; c < kBoxes; ++c)
-        tma_load_2d(s.q + c * (kTileM * 128), &p.tm_q, bar(s, B_QFULL), c * 64,
-                    im.bh * p.n + t.row0);
+        for (int c = 0; c < kBoxes; ++c)
+          tma_load_2d(s.q + c * (kTileM * 128), &p.tm_q, bar(s, B_QFULL), c * 64,
+                      im.bh * p.n + t.row0);
+      } else {
+        for (int i = 0; i < ng; ++i) {
+#pragma unroll
+          for (int c = 0; c < kBoxes; ++c)
+            tma_load_2d(s.q + c * (kTileM * 128) + static_cast<uint32_t>(i * t.gsz) * 128u,
+                        &p.tm_qg, bar(s, B_QFULL), c * 64, im.bh * p.n + t.row0 + i * p.tq);
+        }
+      }
     }
     ++qc;
   };
@@ -687,14 +704,18 @@ __device__ __forceinline__ void load_s(uint32_t sa, uint32_t (&sv)[MAXC][16]) {
 }
 
 // p = 2^(s*c + nb) for the first n16 chunks: stores their bf16 pairs at
-// pa + 8c and adds them to the packed row sums.
-template <int MAXC>
+// pa + 8c and adds them to the packed row sums.  Chunks whose bit in vis is
+// clear (keys the row's frame does not attend, in a merged tail tile) get
+// the bias -inf, so their p is exactly 0.
+template <int MAXC, bool kMasked>
 __device__ __forceinline__ void exp_chunks(const uint32_t (&sv)[MAXC][16], int n16, uint64_t c2,
                                            uint64_t nb2, uint64_t& la, uint64_t& lb,
-                                           uint32_t pa) {
+                                           uint32_t pa, uint32_t vis) {
+  const uint64_t ninf2 = f2_pack(-INFINITY, -INFINITY);
 #pragma unroll
   for (int c = 0; c < MAXC; ++c) {
-    if (c < n16) exp_pack_store(sv[c], c2, nb2, la, lb, pa + 8 * c);
+    if (c < n16)
+      exp_pack_store(sv[c], c2, !kMasked || ((vis >> c) & 1u) ? nb2 : ninf2, la, lb, pa + 8 * c);
   }
 }
 
@@ -715,17 +736,31 @@ struct RowItem {
   }
 };
 
+// Bit c set: chunk f16 + c of the step starting at key block kb (cpb 16-key
+// chunks per block) lies in one of the row's own key runs.
+__device__ __forceinline__ uint32_t chunk_vis(const int (&own)[kGroupInts], int kb, int f16,
+                                              int n16, int cpb) {
+  uint32_t vis = 0;
+  for (int c = 0; c < n16; ++c) {
+    const int b = kb + (f16 + c) / cpb;
+    if ((b >= own[0] && b < own[0] + own[1]) || (b >= own[2] && b < own[2] + own[3]))
+      vis |= 1u << c;
+  }
+  return vis;
+}
+
 __device__ __forceinline__ RowItem row_item(const FwdParams& p, const Item& im,
                                             const WorkTile& t, int r) {
   RowItem x;
   x.im = im;
   x.t = t;
   x.online = p.force_path >= 0 ? (p.force_path == 1) : (p.elig[x.im.bh] == 0);
-  x.grow = static_cast<size_t>(x.im.bh) * p.n + x.t.row0 + r;
+  const int64_t tok = tile_row_token(t, r, p.tq);
+  x.grow = static_cast<size_t>(x.im.bh) * p.n + tok;
   x.valid = r < x.t.nvalid && WSATTN_BOUNDS(p.status, x.grow < static_cast<size_t>(p.bh) * p.n);
   // loads only: their values are first used when the item starts
   x.qn = x.valid ? p.qn_rows[x.grow] : 0.f;
-  x.kq = x.valid ? p.kq[static_cast<size_t>(x.im.bh) * p.nfq + x.t.row0 / p.tq] : 0.f;
+  x.kq = x.valid ? p.kq[static_cast<size_t>(x.im.bh) * p.nfq + tok / p.tq] : 0.f;
   x.c = x.valid ? p.c_rows[x.grow] : 0.f;
   return x;
 }
@@ -769,17 +804,29 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
     st.init(t);
     float l = 0.f;
     float m = -INFINITY;
-    if (!online) {
+    // The step loops, compiled once for ordinary tiles and once for merged
+    // tail tiles (whose rows see only their own frames' key chunks).
+    auto fixed_path = [&](auto masked_tag) -> bool {
+      constexpr bool kMasked = decltype(masked_tag)::value;
+      // merged tail tile: the row's own frame's key runs (rows past the
+      // groups see the whole union)
+      int own[kGroupInts] = {0, 0x3fffffff, 0, 0};
+      if (kMasked && valid) {
+#pragma unroll
+        for (int i = 0; i < kGroupInts; ++i)
+          own[i] = p.grp[static_cast<size_t>(t.gtab + r / t.gsz) * kGroupInts + i];
+      }
       // Fixed max: every step is load, exp, pack, store; the row sum
       // accumulates.
       const uint64_t nb2 = f2_pack(nb_fixed, nb_fixed);
       uint64_t la = f2_pack(0.f, 0.f), lb = la;
       for (int j = 0; j < t.nstep; ++j) {
         int nblk;
-        st.next(G, nblk);
+        const int kb = st.next(G, nblk);
         const int keys = nblk * bk;
         int f16, n16;  // this warpgroup's 16-column chunks of the step
         wg_share(keys / 16, wg, f16, n16);
+        const uint32_t vis = kMasked ? chunk_vis(own, kb, f16, n16, bk / 16) : ~0u;
         const uint32_t c0 = static_cast<uint32_t>(16 * f16);  // first S column
         const uint32_t pb = pr.slot;
         // the S columns read and the P columns written lie in the allocation
@@ -787,7 +834,7 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         const bool cols_ok = WSATTN_BOUNDS(
             p.status, tc_.s + c0 + 16u * MAXC <= kTmemCols && n16 <= MAXC &&
                           c0 / 2 + 8u * n16 <= tc_.pstride && tc_.p + 2u * tc_.pstride <= kTmemCols);
-        if (!wait_warp(s, bar(s, B_SFULL), su)) return;
+        if (!wait_warp(s, bar(s, B_SFULL), su)) return false;
         tc_fence_after();
         uint32_t sv[MAXC][16];
         if (cols_ok) load_s<MAXC>(lane + tc_.s + c0, sv);
@@ -795,10 +842,11 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         warp_arrive(bar(s, B_SEMPTY));
         su ^= 1u;
         // the PV that read this P buffer two steps back must be done
-        if (!wait_warp(s, bar(s, B_PVDONE0 + pb), pr.phase ^ 1u)) return;
+        if (!wait_warp(s, bar(s, B_PVDONE0 + pb), pr.phase ^ 1u)) return false;
         tc_fence_after();
         if (cols_ok)
-          exp_chunks<MAXC>(sv, n16, c2, nb2, la, lb, lane + tc_.p + pb * tc_.pstride + c0 / 2);
+          exp_chunks<MAXC, kMasked>(sv, n16, c2, nb2, la, lb,
+                                    lane + tc_.p + pb * tc_.pstride + c0 / 2, vis);
         tmem_wait_st();
         tc_fence_before();
         warp_arrive(bar(s, B_PFULL0 + pb));
@@ -806,19 +854,31 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
       }
       const float2 a = f2_unpack(f2_add(la, lb));
       l = a.x + a.y;
-    } else {
+      return true;
+    };
+    auto online_path = [&](auto masked_tag) -> bool {
+      constexpr bool kMasked = decltype(masked_tag)::value;
+      // merged tail tile: the row's own frame's key runs (rows past the
+      // groups see the whole union)
+      int own[kGroupInts] = {0, 0x3fffffff, 0, 0};
+      if (kMasked && valid) {
+#pragma unroll
+        for (int i = 0; i < kGroupInts; ++i)
+          own[i] = p.grp[static_cast<size_t>(t.gtab + r / t.gsz) * kGroupInts + i];
+      }
       for (int j = 0; j < t.nstep; ++j) {
         int nblk;
-        st.next(G, nblk);
+        const int kb = st.next(G, nblk);
         const int keys = nblk * bk;
         int f16, n16;
         wg_share(keys / 16, wg, f16, n16);
+        const uint32_t vis = kMasked ? chunk_vis(own, kb, f16, n16, bk / 16) : ~0u;
         const uint32_t c0 = static_cast<uint32_t>(16 * f16);
         const bool cols_ok = WSATTN_BOUNDS(
             p.status, tc_.s + c0 + 16u * MAXC <= kTmemCols && n16 <= MAXC &&
                           c0 / 2 + 8u * n16 <= tc_.pstride && tc_.p + 2u * tc_.pstride <= kTmemCols &&
                           ocol + 16u * nog <= kTmemCols);
-        if (!wait_warp(s, bar(s, B_SFULL), su)) return;
+        if (!wait_warp(s, bar(s, B_SFULL), su)) return false;
         tc_fence_after();
         uint32_t sv[MAXC][16];
         if (cols_ok) {
@@ -836,13 +896,13 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         float mx = -INFINITY;
 #pragma unroll
         for (int k = 0; k < MAXC; ++k) {
-          if (k < n16) {
+          if (k < n16 && (!kMasked || ((vis >> k) & 1u))) {
 #pragma unroll
             for (int i = 0; i < 16; ++i) mx = fmaxf(mx, __uint_as_float(sv[k][i]));
           }
         }
         s.xch_m[(xpar * kNumWG + wg) * kTileM + r] = mx;
-        if (!xch_sync(s, xc)) return;
+        if (!xch_sync(s, xc)) return false;
         float mall = mx;
 #pragma unroll
         for (int v = 0; v < kNumWG; ++v) mall = fmaxf(mall, s.xch_m[(xpar * kNumWG + v) * kTileM + r]);
@@ -855,12 +915,12 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         const float m_new = m_top > m + kLazyMax ? m_top : m;
         const float alpha = m_new == m ? 1.f : ex2_approx(m - m_new);
         const uint32_t pb = pr.slot;
-        if (!wait_warp(s, bar(s, B_PVDONE0 + pb), pr.phase ^ 1u)) return;
+        if (!wait_warp(s, bar(s, B_PVDONE0 + pb), pr.phase ^ 1u)) return false;
         tc_fence_after();
         uint64_t sa2 = f2_pack(0.f, 0.f), sb2 = sa2;
         if (cols_ok)
-          exp_chunks<MAXC>(sv, n16, c2, f2_pack(-m_new, -m_new), sa2, sb2,
-                           lane + tc_.p + pb * tc_.pstride + c0 / 2);
+          exp_chunks<MAXC, kMasked>(sv, n16, c2, f2_pack(-m_new, -m_new), sa2, sb2,
+                           lane + tc_.p + pb * tc_.pstride + c0 / 2, vis);
         const float2 a = f2_unpack(f2_add(sa2, sb2));
         l = l * alpha + (a.x + a.y);
         m = m_new;
@@ -871,7 +931,7 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
           // exact.  Ring position of step j-1: the other slot, same phase
           // when this slot is 1, flipped when it is 0.
           const uint32_t prev_phase = pb == 1u ? pr.phase : pr.phase ^ 1u;
-          if (!wait_warp(s, bar(s, B_PVDONE0 + (pb ^ 1u)), prev_phase)) return;
+          if (!wait_warp(s, bar(s, B_PVDONE0 + (pb ^ 1u)), prev_phase)) return false;
           tc_fence_after();
           const uint64_t a2 = f2_pack(alpha, alpha);
 #pragma unroll 1
@@ -894,7 +954,12 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         warp_arrive(bar(s, B_PFULL0 + pb));
         pr.next(2);
       }
-    }
+        return true;
+    };
+    const bool steps_ok =
+        !online ? (t.gsz ? fixed_path(std::true_type{}) : fixed_path(std::false_type{}))
+                : (t.gsz ? online_path(std::true_type{}) : online_path(std::false_type{}));
+    if (!steps_ok) return;
 
     // Stage the next tile's Q so its first QK products overlap this epilogue,
     // and start the loads of its row parameters.
@@ -930,9 +995,12 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
     const int wq = warp & 3;
     // O's columns lie in the allocation; a full warp's 32 rows in the output
     const bool o_ok = WSATTN_BOUNDS(p.status, ocol + 16u * nog <= kTmemCols);
+    // (in a merged tail tile they are when a row group holds a multiple of
+    // 32 rows)
+    const int64_t wtok = tile_row_token(t, 32 * wq, p.tq);
     const bool warp_full =
-        32 * wq + 32 <= t.nvalid &&
-        WSATTN_BOUNDS(p.status, im.bh * p.n + t.row0 + 32 * wq + 32 <= p.bh * p.n);
+        32 * wq + 32 <= t.nvalid && t.gsz % 32 == 0 &&
+        WSATTN_BOUNDS(p.status, im.bh * p.n + wtok + 32 <= static_cast<int64_t>(p.bh) * p.n);
     const uint32_t chunk = s.ostage + static_cast<uint32_t>(warp - kSoftmaxWarp0) * kOChunkBytes;
     const int lid = threadIdx.x & 31;
 #pragma unroll 1
@@ -954,8 +1022,8 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         fence_proxy_async_smem();
         __syncwarp();
         if (lid == 0) {
-          tma_store_2d_hint(&p.tm_o, chunk, 16 * (og0 + k), im.bh * p.n + t.row0 + 32 * wq,
-                            out_policy);
+          tma_store_2d_hint(&p.tm_o, chunk, 16 * (og0 + k),
+                            static_cast<int32_t>(im.bh * p.n + wtok), out_policy);
           bulk_commit_group();
         }
       } else if (valid) {

@@ -31,16 +31,35 @@ constexpr float kDefaultTau = 40.0f;
 // most two runs of consecutive blocks (the reference frames and the window),
 // so the kernel walks them arithmetically: block j is run0 + j for j < len0,
 // else run1 + (j - len0).
+//
+// When T is not a multiple of 128, each frame ends in a short tail tile of
+// T mod 128 rows.  The tails of up to 128 / (T mod 128) consecutive frames
+// are merged into one tile whose key list is the union of theirs (still at
+// most two runs), when that takes fewer key steps than the separate tails.
+// Row group i (tile rows [i*gsz, (i+1)*gsz)) is the tail of the first
+// frame's successor i, i.e. tokens row0 + i*T onwards.  Its own key runs are
+// in the group table, and the keys of the union that its frame does not
+// attend get probability zero.
 struct WorkTile {
   int32_t row0;    // first query token of the tile (within the head)
-  int32_t nvalid;  // rows of the tile that belong to the frame (<= 128)
-  int32_t nblk;    // active key blocks of the frame
+  int32_t nvalid;  // rows of the tile that belong to its frame(s) (<= 128)
+  int32_t nblk;    // active key blocks of the tile (of the union for merged tails)
   int32_t run0;    // first key block of the first run (units of bk)
   int32_t len0;    // blocks in the first run
   int32_t run1;    // first key block of the second run
   int32_t nstep;   // key steps: ceil(len0 / G) + ceil((nblk - len0) / G)
-  int32_t kbeg;    // first of the frame's blocks in kcol (kcol[kbeg + j], j < nblk)
+  int32_t kbeg;    // first of the (first) frame's blocks in kcol (kcol[kbeg + j])
+  int32_t gsz;     // merged tails: rows per row group; 0 for a tile of one frame
+  int32_t gtab;    // merged tails: first group's entry in the group table
 };
+// Group table entry of a merged tile's row group: its frame's key runs
+// {run0, len0, run1, len1} (units of bk; len1 may be 0).
+constexpr int kGroupInts = 4;
+
+// Token (within the head) of row r of tile t, T tokens per frame.
+__host__ __device__ inline int64_t tile_row_token(const WorkTile& t, int r, int T) {
+  return t.gsz ? t.row0 + static_cast<int64_t>(r / t.gsz) * T + r % t.gsz : t.row0 + r;
+}
 
 // Host-side plan: geometry, block map, and the forward work list.
 struct HostPlan {
@@ -52,6 +71,8 @@ struct HostPlan {
   std::vector<int32_t> col;        // [nnz]
   std::vector<WorkTile> tiles;     // longest first
   std::vector<int32_t> kcol;       // per frame, key block indices (units of bk)
+  std::vector<int32_t> grp;        // group table of merged tail tiles (kGroupInts per group)
+  int gsz = 0;                     // rows per row group of the merged tail tiles (0: none)
   // Tiles with equal key-list length form a class; class c covers tiles
   // [cls[c], cls[c + 1]).  The forward visits work items class by class
   // (longest first) and, inside a class, head by head, so CTAs running at
@@ -147,10 +168,12 @@ void prepare_chunking(int BH, int64_t N, int num_sms, int* nchunk, int* rows_per
 // ------------------------------------------------------------ forward
 struct FwdParams {
   CUtensorMap tm_q;  // [BH*N, D] bf16, box {64, 128}, 128-byte swizzle
+  CUtensorMap tm_qg; // [BH*N, D] bf16, box {64, gsz}: one row group of a merged tail tile
   CUtensorMap tm_k;  // [BH*N, D] bf16, box {64, G * bk}
   CUtensorMap tm_v;  // [BH*N, D] bf16, box {64, G * bk}
   CUtensorMap tm_o;  // [BH*N, D] fp32, box {16, 32}, no swizzle (epilogue stores)
   const WorkTile* tiles;
+  const int32_t* grp;    // group table of the merged tail tiles
   const int32_t* cls;    // class boundaries into tiles, n_cls + 1 entries
   int* work;             // [2]: next work item, CTAs finished (both 0 between launches)
   int n_cls;

@@ -15,12 +15,49 @@
 // reference keys.
 #include <algorithm>
 #include <new>
+#include <utility>
 
 #include "internal.h"
 
 namespace wsattn {
 
 static bool valid_block(int b, int T) { return b >= 16 && b % 16 == 0 && T % b == 0; }
+
+namespace {
+
+// A frame's key blocks: at most two runs of consecutive blocks.
+struct FrameKeys {
+  int64_t frame;
+  int32_t kbeg, nblk;
+  int32_t run[2], len[2];
+};
+
+int32_t key_steps(int32_t len0, int32_t len1, int G) { return (len0 + G - 1) / G + (len1 + G - 1) / G; }
+
+// The union of the key blocks of f[0 .. m), as at most two runs; false if it
+// takes more.
+bool union_runs(const FrameKeys* f, int m, int32_t (&run)[2], int32_t (&len)[2]) {
+  std::vector<std::pair<int32_t, int32_t>> iv;  // [begin, end)
+  for (int i = 0; i < m; ++i)
+    for (int r = 0; r < 2; ++r)
+      if (f[i].len[r] > 0) iv.emplace_back(f[i].run[r], f[i].run[r] + f[i].len[r]);
+  std::sort(iv.begin(), iv.end());
+  std::vector<std::pair<int32_t, int32_t>> u;
+  for (const auto& x : iv) {
+    if (!u.empty() && x.first <= u.back().second)
+      u.back().second = std::max(u.back().second, x.second);
+    else
+      u.push_back(x);
+  }
+  if (u.empty() || u.size() > 2) return false;
+  run[0] = u[0].first;
+  len[0] = u[0].second - u[0].first;
+  run[1] = u.size() == 2 ? u[1].first : 0;
+  len[1] = u.size() == 2 ? u[1].second - u[1].first : 0;
+  return true;
+}
+
+}  // namespace
 
 // The forward kernel streams keys in steps of floor(kStepKeys / bk) blocks,
 // so the automatic size is the valid block whose step holds the most keys;
@@ -90,8 +127,11 @@ int build_host_plan(int frames, int tokens_per_frame, int window, int ref_frames
 
     // Work list: every 128-row query tile of every frame, with the frame's key
     // blocks.  The key list of frame a is the CSR row of its first q-block
-    // (all q-blocks of a frame share it).
+    // (all q-blocks of a frame share it).  Frames' short tail tiles are
+    // collected and merged below.
     const int tiles_per_frame = (T + kTileM - 1) / kTileM;
+    const int tail = T % kTileM;
+    std::vector<FrameKeys> tails;
     for (int64_t a = 0; a < nf; ++a) {
       const int64_t qb0 = a * T / bq;
       const int32_t kbeg = static_cast<int32_t>(p.kcol.size());
@@ -115,17 +155,65 @@ int build_host_plan(int frames, int tokens_per_frame, int window, int ref_frames
       }
       if (nrun == 0) return WSATTN_ERR_BAD_ARG;  // every frame sees at least itself
       for (int t = 0; t < tiles_per_frame; ++t) {
-        WorkTile wt;
+        if (tail && t == tiles_per_frame - 1) {
+          tails.push_back(FrameKeys{a, kbeg, kend - kbeg, {run[0], nrun == 2 ? run[1] : 0},
+                                    {len[0], len[1]}});
+          continue;
+        }
+        WorkTile wt{};
         wt.row0 = static_cast<int32_t>(a * T + t * kTileM);
         wt.nvalid = std::min(kTileM, T - t * kTileM);
         wt.nblk = kend - kbeg;
         wt.run0 = run[0];
         wt.len0 = len[0];
         wt.run1 = nrun == 2 ? run[1] : 0;
-        wt.nstep = (len[0] + p.G - 1) / p.G + (len[1] + p.G - 1) / p.G;
+        wt.nstep = key_steps(len[0], len[1], p.G);
         wt.kbeg = kbeg;
         p.tiles.push_back(wt);
       }
+    }
+    // Tail tiles: up to g = 128 / tail consecutive frames' tails share one
+    // tile when the union of their key blocks is still two runs at most and
+    // takes fewer key steps than the tails one by one (greedily, in token
+    // order).  The first group's rows are the first frame's tail.
+    const int g = tail ? kTileM / tail : 0;
+    for (size_t i = 0; i < tails.size();) {
+      int m = static_cast<int>(std::min<size_t>(static_cast<size_t>(g), tails.size() - i));
+      int32_t urun[2] = {0, 0}, ulen[2] = {0, 0};
+      for (; m >= 2; --m) {
+        int32_t sep = 0;
+        for (int j = 0; j < m; ++j) sep += key_steps(tails[i + j].len[0], tails[i + j].len[1], p.G);
+        if (union_runs(&tails[i], m, urun, ulen) && key_steps(ulen[0], ulen[1], p.G) < sep) break;
+      }
+      const FrameKeys& f0 = tails[i];
+      WorkTile wt{};
+      wt.row0 = static_cast<int32_t>(f0.frame * T + (tiles_per_frame - 1) * kTileM);
+      wt.kbeg = f0.kbeg;
+      if (m >= 2) {
+        wt.nvalid = m * tail;
+        wt.nblk = ulen[0] + ulen[1];
+        wt.run0 = urun[0];
+        wt.len0 = ulen[0];
+        wt.run1 = urun[1];
+        wt.nstep = key_steps(ulen[0], ulen[1], p.G);
+        wt.gsz = tail;
+        wt.gtab = static_cast<int32_t>(p.grp.size() / kGroupInts);
+        for (int j = 0; j < m; ++j) {
+          const FrameKeys& f = tails[i + j];
+          p.grp.insert(p.grp.end(), {f.run[0], f.len[0], f.run[1], f.len[1]});
+        }
+        p.gsz = tail;
+        i += static_cast<size_t>(m);
+      } else {
+        wt.nvalid = tail;
+        wt.nblk = f0.nblk;
+        wt.run0 = f0.run[0];
+        wt.len0 = f0.len[0];
+        wt.run1 = f0.run[1];
+        wt.nstep = key_steps(f0.len[0], f0.len[1], p.G);
+        ++i;
+      }
+      p.tiles.push_back(wt);
     }
     // Longest first (the reference frame's tiles see every key block); the
     // order among equal lengths stays the token order.

@@ -229,10 +229,34 @@ int wsattn_prepare_static(int batch, int heads, int n_tokens, int head_dim, floa
 /* ---------------------------------------------------------- introspection */
 
 /* Plan geometry.  info[0..9] = N, block_q, block_k, q blocks, k blocks,
- * active blocks (CSR nnz), work tiles per (b, h) (128-row query tiles),
+ * active blocks (CSR nnz), work tiles per (b, h) (128-row query tiles,
+ * with consecutive frames' short tails merged; see wsattn_get_tiles),
  * head_dim, heads, active (query, key) element pairs per (b, h).  n is the
  * capacity of info; at most n entries are written. */
 int wsattn_plan_info(wsattn_plan_t plan, int64_t* info, int n);
+
+/* Copies the forward work list (in its execution order) into host memory:
+ * 10 int32 per tile, {row0, nvalid, nblk, run0, len0, run1, nstep, kbeg,
+ * gsz, gtab}, and the group table of the merged tail tiles, 4 int32 per
+ * row group {run0, len0, run1, len1}.  Key runs are in units of block_k.
+ * Rows are query tokens within a head.  A tile with gsz = 0 covers tokens
+ * [row0, row0 + nvalid) of one frame, with that frame's key blocks: run0 ..
+ * run0 + len0 - 1, then run1 .. run1 + nblk - len0 - 1.
+ * Frames whose token span T is not a multiple of 128 end in a short tail
+ * tile.  A tile with gsz > 0 merges consecutive frames' tails ("Deleting the
+ * mask" of the Google Developers Blog post "HeyGen x Google Cloud: Bringing
+ * Avatar IV to TPUs" streams only active key blocks; merging the tails keeps
+ * a frame's short last tile from costing a whole tile's key steps):
+ *   - its row group i holds tile rows [i*gsz, (i+1)*gsz), which are tokens
+ *     row0 + i*T .. row0 + i*T + gsz - 1;
+ *   - the tile walks the union of the groups' key blocks;
+ *   - group i's own blocks are entry gtab + i of the group table.
+ * n_tiles and n_groups are capacities in int32 (n_tiles >= 10 x work
+ * tiles per (b, h) from wsattn_plan_info; n_groups >= 4 x row groups; both
+ * pointers may be NULL when the count is zero).
+ * Errors: BAD_ARG if a capacity is too small. */
+int wsattn_get_tiles(wsattn_plan_t plan, int32_t* tiles, size_t n_tiles, int32_t* groups,
+                     size_t n_groups);
 
 /* Copies the block bitmap (row-major [N/block_q, N/block_k], 1 = active)
  * into host memory of n bytes.  Errors: BAD_ARG if n is too small. */

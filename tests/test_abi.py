@@ -55,7 +55,73 @@ def _plan_vs_oracle(F, T, w, R, bq, bk, flags=0):
     assert plan.nnz == want["nnz"]
     m_pairs = oracle.blockmap(F, T, w, R, T, T, flags)["nnz"] * T * T
     assert plan.active_pairs == m_pairs
-    assert plan.tiles_per_head == (F + R) * ((T + 127) // 128)
+    _check_work_list(plan, F, T, w, R, bk, flags)
+    plan.destroy()
+
+
+def _runs_set(run0, len0, run1, len1):
+    return set(range(run0, run0 + len0)) | set(range(run1, run1 + len1))
+
+
+def _check_work_list(plan, F, T, w, R, bk, flags=0):
+    """The forward work list against the oracle's frame-level block map
+    (query block = one frame): every query token lies in exactly one tile
+    row, and each row's own key blocks are its frame's.  A merged tail tile
+    (gsz > 0) walks the union of its row groups' blocks."""
+    import frame_aligned_window_gb300 as fw
+    tiles, groups = fw.wsattn_get_tiles(plan)
+    assert len(tiles) == plan.tiles_per_head
+    frame_keys = oracle.blockmap(F, T, w, R, T, bk, flags)["bitmap"]  # [F+R, N/bk]
+    N = (F + R) * T
+    seen = np.zeros(N, dtype=np.int32)
+    tail = T % 128
+    n_merged = 0
+    for row0, nvalid, nblk, run0, len0, run1, nstep, kbeg, gsz, gtab in tiles:
+        assert 0 < nvalid <= 128 and nblk == len0 + (nblk - len0) and nstep > 0
+        walk = _runs_set(run0, len0, run1, nblk - len0)
+        assert len(walk) == nblk
+        if gsz == 0:
+            toks = np.arange(row0, row0 + nvalid)
+            frames = toks // T
+            assert (frames == frames[0]).all()
+            want = set(np.flatnonzero(frame_keys[frames[0]]))
+            assert walk == want, (row0, nvalid)
+        else:
+            n_merged += 1
+            assert gsz == tail and nvalid % gsz == 0 and nvalid // gsz >= 2
+            union = set()
+            toks = []
+            for i in range(nvalid // gsz):
+                g = groups[gtab + i]
+                own = _runs_set(*g)
+                t0 = row0 + i * T
+                f = t0 // T
+                assert (t0 + gsz - 1) // T == f and (t0 % T) == T - tail
+                assert own == set(np.flatnonzero(frame_keys[f])), (row0, i)
+                union |= own
+                toks.extend(range(t0, t0 + gsz))
+            assert walk == union
+            toks = np.array(toks)
+        seen[toks] += 1
+    assert (seen == 1).all()
+    if tail == 0:
+        assert n_merged == 0 and plan.tiles_per_head == (F + R) * (T // 128)
+    else:
+        assert plan.tiles_per_head <= (F + R) * ((T + 127) // 128)
+
+
+@pytest.mark.parametrize("name", ["sr", "sr_long", "dense"])
+def test_work_list_merges_frame_tails(name):
+    # T mod 128 = 16 (SR) or 32 (SR-long, dense): consecutive frames' tails
+    # share tiles, and every row still walks exactly its frame's key blocks
+    import frame_aligned_window_gb300 as fw
+    wl = WORKLOADS[name]
+    plan = fw.wsattn_plan(wl.frames, wl.tokens_per_frame, wl.window, wl.ref_frames, wl.heads,
+                          wl.head_dim)
+    _check_work_list(plan, wl.frames, wl.tokens_per_frame, wl.window, wl.ref_frames,
+                     plan.block_k)
+    tiles, groups = fw.wsattn_get_tiles(plan)
+    assert (tiles[:, 8] > 0).any() and len(groups) > 0
     plan.destroy()
 
 
