@@ -191,6 +191,27 @@ def test_edge_shapes_full_parity(case):
     _full_compare(wl, q, k, v, out)
 
 
+@pytest.mark.parametrize("force_path", [-1, 1])
+def test_merged_tails_ignore_keys_outside_the_row_frame(force_path):
+    # T = 144: every frame ends in a 16-row tail, and the tails of eight
+    # consecutive frames share one tile whose key list is the union of
+    # theirs.  Head 0's keys of video frame 9 (token frame 10) are scaled by
+    # 8, so their logits dwarf every other's: a row of a frame that does not
+    # attend frame 9 but shares a merged tile with one that does gets the
+    # wrong answer if those keys leak into its probabilities or (online
+    # path) its running max.  Head 0 becomes ineligible (online path), head 1
+    # stays on the fixed path unless forced.
+    import frame_aligned_window_gb300 as fw
+    wl, q, k, v = micro(59, 1, 2, 128, 12, 1, 144, 1)
+    T = wl.tokens_per_frame
+    k = k.clone()
+    k[0, 0, 10 * T:11 * T] = (k[0, 0, 10 * T:11 * T].float() * 8).to(torch.bfloat16)
+    plan, out, _ = gpu_run(wl, q, k, v, force_path=force_path)
+    tiles, groups = fw.wsattn_get_tiles(plan)
+    assert (tiles[:, 8] == 16).any()
+    _full_compare(wl, q, k, v, out)
+
+
 def test_degenerate_inputs():
     wl, q, k, v = micro(56, 1, 2, 128, 4, 1, 96, 1)
     # zero queries: every row is the mean of the values it sees

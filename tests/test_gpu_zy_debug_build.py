@@ -26,6 +26,7 @@ IN_CHILD = os.environ.get("WSATTN_EXPECT_DEBUG") == "1"
 RERUN = [
     "tests/test_gpu_forward.py::test_forward_full_parity",
     "tests/test_gpu_forward.py::test_edge_shapes_full_parity",
+    "tests/test_gpu_forward.py::test_merged_tails_ignore_keys_outside_the_row_frame",
     "tests/test_gpu_forward.py::test_block_sizes_tiny",
     "tests/test_gpu_forward.py::test_block_sizes_dense_frame_span",
     "tests/test_gpu_forward.py::test_block_sizes_step_buffers",
