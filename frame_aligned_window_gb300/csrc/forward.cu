@@ -5,6 +5,11 @@
 //   - "Deleting the mask" (Fig. 3): key blocks divide the frame span, so each
 //     query tile visits only fully active key blocks -- reference frame and
 //     window alike, in one pass -- with no mask predicate and no padding.
+//     Frames whose token span is not a multiple of 128 end in short tails;
+//     consecutive frames' tails share one tile whose key list is the union
+//     of theirs.  There, and only there, a row zeroes the 16-key chunks of
+//     the union that its own frame does not attend (still whole chunks of
+//     fully active or skipped blocks, never single elements).
 //   - "Breaking softmax's dependency chain" (Fig. 4): on eligible heads the
 //     row bound is the softmax max, so a block's probabilities are
 //     p = exp(scale*s - m_i) with no running max and no rescale in the loop
@@ -985,18 +990,17 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
     tc_fence_after();
     const float inv = 1.f / lsum;
     float* orow = p.out + grow * D + 16 * og0;
-    // A warp whose 32 rows all belong to the frame stages each 16-column group
-    // in its shared chunk (its rows 64 bytes apart) and sends it with one TMA
-    // store: the per-thread row stores below touch 32 rows per instruction.
-    // The chunk uses the 64-byte swizzle (16-byte unit u of row r sits at unit
+    // A warp whose 32 rows are 32 consecutive output tokens (every full warp
+    // of an ordinary tile; in a merged tail tile, when its row groups hold a
+    // multiple of 32 rows) stages each 16-column group in its shared chunk
+    // (its rows 64 bytes apart) and sends it with one TMA store: the
+    // per-thread row stores below touch 32 rows per instruction.  The chunk
+    // uses the 64-byte swizzle (16-byte unit u of row r sits at unit
     // u ^ ((r >> 1) & 3)), so each quarter-warp's 16-byte stores fall in eight
-    // different bank groups.  Warps of a frame's tail tile store their valid
-    // rows themselves.
+    // different bank groups.  Other warps store their valid rows themselves.
     const int wq = warp & 3;
     // O's columns lie in the allocation; a full warp's 32 rows in the output
     const bool o_ok = WSATTN_BOUNDS(p.status, ocol + 16u * nog <= kTmemCols);
-    // (in a merged tail tile they are when a row group holds a multiple of
-    // 32 rows)
     const int64_t wtok = tile_row_token(t, 32 * wq, p.tq);
     const bool warp_full =
         32 * wq + 32 <= t.nvalid && t.gsz % 32 == 0 &&
