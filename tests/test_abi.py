@@ -125,6 +125,34 @@ def test_work_list_merges_frame_tails(name):
     plan.destroy()
 
 
+def test_get_tiles_checks_capacities():
+    import frame_aligned_window_gb300 as fw
+    wl = WORKLOADS["sr"]
+    plan = fw.wsattn_plan(wl.frames, wl.tokens_per_frame, wl.window, wl.ref_frames, wl.heads,
+                          wl.head_dim)
+    tiles, groups = fw.wsattn_get_tiles(plan)
+    fn = fw.raw_call("wsattn_get_tiles")
+    t = np.zeros(tiles.size, dtype=np.int32)
+    g = np.zeros(groups.size, dtype=np.int32)
+    tp, gp = ctypes.c_void_p(t.ctypes.data), ctypes.c_void_p(g.ctypes.data)
+    assert fn(plan.handle, tp, t.size, gp, g.size) == 0
+    np.testing.assert_array_equal(t.reshape(tiles.shape), tiles)
+    np.testing.assert_array_equal(g.reshape(groups.shape), groups)
+    assert fn(plan.handle, tp, t.size - 1, gp, g.size) == 1   # one int short: BAD_ARG
+    assert fn(plan.handle, tp, t.size, gp, g.size - 1) == 1
+    assert fn(plan.handle, None, t.size, gp, g.size) == 1
+    assert fn(plan.handle, tp, t.size, None, g.size) == 1
+    assert fn(None, tp, t.size, gp, g.size) == 1
+    plan.destroy()
+    # no merged tiles (T a multiple of 128): an empty group table, NULL allowed
+    plan = fw.wsattn_plan(3, 256, 1, 1, 2, 128)
+    tiles, groups = fw.wsattn_get_tiles(plan)
+    assert len(groups) == 0 and (tiles[:, 8] == 0).all() and len(tiles) == 4 * 2
+    t = np.zeros(tiles.size, dtype=np.int32)
+    assert fn(plan.handle, ctypes.c_void_p(t.ctypes.data), t.size, None, 0) == 0
+    plan.destroy()
+
+
 @pytest.mark.parametrize("name", ["tiny", "small"])
 def test_plan_matches_oracle_all_valid_sizes(name):
     wl = WORKLOADS[name]
