@@ -125,6 +125,26 @@ def test_work_list_merges_frame_tails(name):
     plan.destroy()
 
 
+def test_work_list_random_shapes():
+    # seeded random shapes: frame counts, token spans with every tail size
+    # (T mod 128 in 16 .. 112, or none), windows, reference frames, all
+    # mask flags and random valid block sizes; the work list must cover each
+    # token once with its own frame's key blocks
+    import frame_aligned_window_gb300 as fw
+    rng = np.random.default_rng(20261202)
+    for _ in range(60):
+        F = int(rng.integers(1, 14))
+        R = int(rng.integers(0, 3))
+        T = 16 * int(rng.integers(1, 30))
+        w = int(rng.integers(0, 5))
+        flags = int(rng.integers(0, 8))
+        blocks = valid_blocks(T, 160)
+        bk = int(rng.choice(blocks))
+        plan = fw.wsattn_plan(F, T, w, R, 2, 128, 0, bk, flags)
+        _check_work_list(plan, F, T, w, R, bk, flags)
+        plan.destroy()
+
+
 def test_get_tiles_checks_capacities():
     import frame_aligned_window_gb300 as fw
     wl = WORKLOADS["sr"]
