@@ -42,6 +42,26 @@ def test_variant_forward_online_and_d64(flags):
     _full_check(wl, q, k, v, out, flags)
 
 
+@pytest.mark.parametrize("case", range(8))
+def test_random_shapes_full_parity(case):
+    # seeded random shapes (tail sizes, windows, reference frames, mask
+    # flags, head dims and block sizes), so merged tail tiles meet varied
+    # groupings; both paths, every row against the oracle
+    rng = np.random.default_rng(7000 + case)
+    D = int(rng.choice([64, 128]))
+    F = int(rng.integers(2, 9))
+    R = int(rng.integers(0, 3))
+    T = 16 * int(rng.integers(1, 21))
+    w = int(rng.integers(0, 4))
+    flags = int(rng.integers(0, 8))
+    bk = int(rng.choice([b for b in range(16, min(T, 160) + 1, 16) if T % b == 0]))
+    wl, q, k, v = micro(7000 + case, 1, 2, D, F, R, T, w)
+    _, out, _ = gpu_run(wl, q, k, v, block_k=bk, mask_flags=flags)
+    _full_check(wl, q, k, v, out, flags)
+    _, out, _ = gpu_run(wl, q, k, v, block_k=bk, mask_flags=flags, force_path=1)
+    _full_check(wl, q, k, v, out, flags)
+
+
 @pytest.mark.parametrize("flags", [1, 3])
 def test_variant_long_frames_sampled(flags):
     # SR frame span (T = 1040, 80-key blocks, 160-key steps) with a causal

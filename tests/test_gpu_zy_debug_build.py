@@ -33,6 +33,7 @@ RERUN = [
     "tests/test_gpu_forward.py::test_degenerate_inputs",
     "tests/test_gpu_forward.py::test_batch_mismatch_and_status",
     "tests/test_gpu_mask_variants.py::test_variant_forward_full_parity",
+    "tests/test_gpu_mask_variants.py::test_random_shapes_full_parity",
     "tests/test_gpu_mask_variants.py::test_variant_forward_online_and_d64",
     "tests/test_gpu_mask_variants.py::test_variant_window_bounds",
     "tests/test_gpu_window_bound.py::test_window_bound_flips_eligibility_and_forward_matches",
