@@ -414,6 +414,8 @@ int wsattn_forward(wsattn_plan_t plan, int batch, const void* q, const void* k, 
       (hp.gsz > 0 && !encode_map(&prm.tm_qg, q, rows, hp.D, hp.gsz)) ||
       !encode_map(&prm.tm_k, k, rows, hp.D, step_keys) ||
       !encode_map(&prm.tm_v, v, rows, hp.D, step_keys) ||
+      !encode_map(&prm.tm_k1, k, rows, hp.D, hp.bk) ||
+      !encode_map(&prm.tm_v1, v, rows, hp.D, hp.bk) ||
       !encode_out_map(&prm.tm_o, out, rows, hp.D))
     return WSATTN_ERR_CUDA;
   prm.tiles = plan->d_tiles;

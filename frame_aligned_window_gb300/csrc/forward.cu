@@ -323,35 +323,39 @@ struct Ring {
   }
 };
 
-// Walks a tile's key steps: up to G consecutive blocks of the first run, then
-// of the second.
+// Walks a tile's key blocks G at a time: the first run's blocks, then the
+// second's, as one sequence, so a step may end the first run and start the
+// second (no half-empty step at the end of the first run).
 struct Steps {
-  int kb, left, run1, len1;
+  int j, nblk, run0, len0, run1;
   __device__ __forceinline__ void init(const WorkTile& t) {
-    kb = t.run0;
-    left = t.len0;
+    j = 0;
+    nblk = t.nblk;
+    run0 = t.run0;
+    len0 = t.len0;
     run1 = t.run1;
-    len1 = t.nblk - t.len0;
   }
-  // First block of the next step; nb receives its block count.
+  // Key block at walk position i.
+  __device__ __forceinline__ int block(int i) const { return i < len0 ? run0 + i : run1 + (i - len0); }
+  // Walk position of the next step's first block; nb receives its block count.
   __device__ __forceinline__ int next(int G, int& nb) {
-    if (left == 0) {
-      kb = run1;
-      left = len1;
-      len1 = 0;
-    }
-    nb = left < G ? left : G;
-    const int first = kb;
-    kb += nb;
-    left -= nb;
+    const int first = j;
+    nb = nblk - j < G ? nblk - j : G;
+    j += nb;
     return first;
+  }
+  // Whether the step at walk position `first` with nb blocks spans both runs.
+  __device__ __forceinline__ bool spans(int first, int nb) const {
+    return first < len0 && first + nb > len0;
   }
 };
 
 // ------------------------------------------------------------------ producer
-// A step's G blocks are consecutive rows of one run, so each step is one TMA
-// box per 64-column slab (G * bk rows).  The shorter last step of a run
-// loads the whole box too: the rows past it are never read by an MMA.
+// A step's G blocks are normally consecutive rows of one run, so the step is
+// one TMA box per 64-column slab (G * bk rows).  The shorter last step of a
+// tile loads the whole box too: the rows past it are never read by an MMA.
+// A step that ends the first run and starts the second is loaded one block
+// (bk rows) per box into consecutive rows of the stage.
 // After an expired wait: the TMA loads this producer issued land in shared
 // memory whatever the consumers do, so wait (bounded) for each slot's last
 // load before the CTA may leave.
@@ -453,18 +457,32 @@ __device__ void producer_qk(const FwdParams& p, const Shared& s) {
         nq_pending = false;
       }
       int nb;
-      const int row = y0 + ks.next(G, nb) * bk;
+      const int first = ks.next(G, nb);
+      const bool split = ks.spans(first, nb);
+      const int row = y0 + ks.block(first) * bk;
       if (!wait(s, bar(s, B_KEMPTY0 + kr.slot), kr.phase ^ 1u, kStatusTimeoutProducer))
         return drain();
       const uint32_t fb = bar(s, B_KFULL0 + kr.slot);
-      mbar_arrive_expect_tx(fb, stage_bytes);
+      mbar_arrive_expect_tx(fb, split ? static_cast<uint32_t>(nb * bk) * 128u * kBoxes : stage_bytes);
       const uint32_t dst = s.k + kr.slot * stage_bytes;
-      // the step's keys lie in the head (rows past them, to the box end, are
-      // loaded but never read)
-      if (WSATTN_BOUNDS(p.status, nb >= 1 && nb <= G && row >= y0 && row + nb * bk <= y0 + p.n &&
-                                      row + nb * bk <= rows)) {
+      if (!split) {
+        // the step's keys lie in the head (rows past them, to the box end,
+        // are loaded but never read)
+        if (WSATTN_BOUNDS(p.status, nb >= 1 && nb <= G && row >= y0 && row + nb * bk <= y0 + p.n &&
+                                        row + nb * bk <= rows)) {
 #pragma unroll
-        for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_k, fb, c * 64, row);
+          for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_k, fb, c * 64, row);
+        }
+      } else {
+        for (int i = 0; i < nb; ++i) {
+          const int bro = y0 + ks.block(first + i) * bk;
+          if (WSATTN_BOUNDS(p.status, nb <= G && bro >= y0 && bro + bk <= y0 + p.n)) {
+#pragma unroll
+            for (int c = 0; c < kBoxes; ++c)
+              tma_load_2d(dst + c * box_pitch + static_cast<uint32_t>(i * bk) * 128u, &p.tm_k1, fb,
+                          c * 64, bro);
+          }
+        }
       }
       kph = (kph & ~(1u << kr.slot)) | (kr.phase << kr.slot);
       kiss |= 1u << kr.slot;
@@ -500,15 +518,29 @@ __device__ void producer_v(const FwdParams& p, const Shared& s) {
     vs.init(t);
     for (int j = 0; j < t.nstep; ++j) {
       int nb;
-      const int row = y0 + vs.next(G, nb) * bk;
+      const int first = vs.next(G, nb);
+      const bool split = vs.spans(first, nb);
+      const int row = y0 + vs.block(first) * bk;
       if (!wait(s, bar(s, B_VEMPTY0 + vr.slot), vr.phase ^ 1u, kStatusTimeoutProducer))
         return drain();
       const uint32_t fb = bar(s, B_VFULL0 + vr.slot);
-      mbar_arrive_expect_tx(fb, stage_bytes);
+      mbar_arrive_expect_tx(fb, split ? static_cast<uint32_t>(nb * bk) * 128u * kBoxes : stage_bytes);
       const uint32_t dst = s.v + vr.slot * stage_bytes;
-      if (WSATTN_BOUNDS(p.status, nb >= 1 && nb <= G && row >= y0 && row + nb * bk <= y0 + p.n)) {
+      if (!split) {
+        if (WSATTN_BOUNDS(p.status, nb >= 1 && nb <= G && row >= y0 && row + nb * bk <= y0 + p.n)) {
 #pragma unroll
-        for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_v, fb, c * 64, row);
+          for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_v, fb, c * 64, row);
+        }
+      } else {
+        for (int i = 0; i < nb; ++i) {
+          const int bro = y0 + vs.block(first + i) * bk;
+          if (WSATTN_BOUNDS(p.status, nb <= G && bro >= y0 && bro + bk <= y0 + p.n)) {
+#pragma unroll
+            for (int c = 0; c < kBoxes; ++c)
+              tma_load_2d(dst + c * box_pitch + static_cast<uint32_t>(i * bk) * 128u, &p.tm_v1, fb,
+                          c * 64, bro);
+          }
+        }
       }
       vph = (vph & ~(1u << vr.slot)) | (vr.phase << vr.slot);
       viss |= 1u << vr.slot;
@@ -741,13 +773,13 @@ struct RowItem {
   }
 };
 
-// Bit c set: chunk f16 + c of the step starting at key block kb (cpb 16-key
-// chunks per block) lies in one of the row's own key runs.
-__device__ __forceinline__ uint32_t chunk_vis(const int (&own)[kGroupInts], int kb, int f16,
-                                              int n16, int cpb) {
+// Bit c set: chunk f16 + c of the step starting at walk position `first`
+// (cpb 16-key chunks per block) lies in one of the row's own key runs.
+__device__ __forceinline__ uint32_t chunk_vis(const int (&own)[kGroupInts], const Steps& st,
+                                              int first, int f16, int n16, int cpb) {
   uint32_t vis = 0;
   for (int c = 0; c < n16; ++c) {
-    const int b = kb + (f16 + c) / cpb;
+    const int b = st.block(first + (f16 + c) / cpb);
     if ((b >= own[0] && b < own[0] + own[1]) || (b >= own[2] && b < own[2] + own[3]))
       vis |= 1u << c;
   }
@@ -831,7 +863,7 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         const int keys = nblk * bk;
         int f16, n16;  // this warpgroup's 16-column chunks of the step
         wg_share(keys / 16, wg, f16, n16);
-        const uint32_t vis = kMasked ? chunk_vis(own, kb, f16, n16, bk / 16) : ~0u;
+        const uint32_t vis = kMasked ? chunk_vis(own, st, kb, f16, n16, bk / 16) : ~0u;
         const uint32_t c0 = static_cast<uint32_t>(16 * f16);  // first S column
         const uint32_t pb = pr.slot;
         // the S columns read and the P columns written lie in the allocation
@@ -877,7 +909,7 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
         const int keys = nblk * bk;
         int f16, n16;
         wg_share(keys / 16, wg, f16, n16);
-        const uint32_t vis = kMasked ? chunk_vis(own, kb, f16, n16, bk / 16) : ~0u;
+        const uint32_t vis = kMasked ? chunk_vis(own, st, kb, f16, n16, bk / 16) : ~0u;
         const uint32_t c0 = static_cast<uint32_t>(16 * f16);
         const bool cols_ok = WSATTN_BOUNDS(
             p.status, tc_.s + c0 + 16u * MAXC <= kTmemCols && n16 <= MAXC &&

@@ -47,7 +47,7 @@ struct WorkTile {
   int32_t run0;    // first key block of the first run (units of bk)
   int32_t len0;    // blocks in the first run
   int32_t run1;    // first key block of the second run
-  int32_t nstep;   // key steps: ceil(len0 / G) + ceil((nblk - len0) / G)
+  int32_t nstep;   // key steps: ceil(nblk / G) (the runs walked as one sequence)
   int32_t kbeg;    // first of the (first) frame's blocks in kcol (kcol[kbeg + j])
   int32_t gsz;     // merged tails: rows per row group; 0 for a tile of one frame
   int32_t gtab;    // merged tails: first group's entry in the group table
@@ -171,6 +171,8 @@ struct FwdParams {
   CUtensorMap tm_qg; // [BH*N, D] bf16, box {64, gsz}: one row group of a merged tail tile
   CUtensorMap tm_k;  // [BH*N, D] bf16, box {64, G * bk}
   CUtensorMap tm_v;  // [BH*N, D] bf16, box {64, G * bk}
+  CUtensorMap tm_k1; // [BH*N, D] bf16, box {64, bk}: one block of a step that spans both runs
+  CUtensorMap tm_v1; // [BH*N, D] bf16, box {64, bk}
   CUtensorMap tm_o;  // [BH*N, D] fp32, box {16, 32}, no swizzle (epilogue stores)
   const WorkTile* tiles;
   const int32_t* grp;    // group table of the merged tail tiles

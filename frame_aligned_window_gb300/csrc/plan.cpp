@@ -32,7 +32,9 @@ struct FrameKeys {
   int32_t run[2], len[2];
 };
 
-int32_t key_steps(int32_t len0, int32_t len1, int G) { return (len0 + G - 1) / G + (len1 + G - 1) / G; }
+// Key steps of a tile: its two runs are walked as one sequence of blocks,
+// G at a time (a step may end the first run and start the second).
+int32_t key_steps(int32_t len0, int32_t len1, int G) { return (len0 + len1 + G - 1) / G; }
 
 // The union of the key blocks of f[0 .. m), as at most two runs; false if it
 // takes more.
