@@ -336,7 +336,9 @@ struct Steps {
     run1 = t.run1;
   }
   // Key block at walk position i.
-  __device__ __forceinline__ int block(int i) const { return i < len0 ? run0 + i : run1 + (i - len0); }
+  __device__ __forceinline__ int block(int i) const {
+    return i < len0 ? run0 + i : run1 + (i - len0);
+  }
   // Walk position of the next step's first block; nb receives its block count.
   __device__ __forceinline__ int next(int G, int& nb) {
     const int first = j;
@@ -463,7 +465,8 @@ __device__ void producer_qk(const FwdParams& p, const Shared& s) {
       if (!wait(s, bar(s, B_KEMPTY0 + kr.slot), kr.phase ^ 1u, kStatusTimeoutProducer))
         return drain();
       const uint32_t fb = bar(s, B_KFULL0 + kr.slot);
-      mbar_arrive_expect_tx(fb, split ? static_cast<uint32_t>(nb * bk) * 128u * kBoxes : stage_bytes);
+      const uint32_t tx = split ? static_cast<uint32_t>(nb * bk) * 128u * kBoxes : stage_bytes;
+      mbar_arrive_expect_tx(fb, tx);
       const uint32_t dst = s.k + kr.slot * stage_bytes;
       if (!split) {
         // the step's keys lie in the head (rows past them, to the box end,
@@ -471,7 +474,8 @@ __device__ void producer_qk(const FwdParams& p, const Shared& s) {
         if (WSATTN_BOUNDS(p.status, nb >= 1 && nb <= G && row >= y0 && row + nb * bk <= y0 + p.n &&
                                         row + nb * bk <= rows)) {
 #pragma unroll
-          for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_k, fb, c * 64, row);
+          for (int c = 0; c < kBoxes; ++c)
+            tma_load_2d(dst + c * box_pitch, &p.tm_k, fb, c * 64, row);
         }
       } else {
         for (int i = 0; i < nb; ++i) {
@@ -524,12 +528,14 @@ __device__ void producer_v(const FwdParams& p, const Shared& s) {
       if (!wait(s, bar(s, B_VEMPTY0 + vr.slot), vr.phase ^ 1u, kStatusTimeoutProducer))
         return drain();
       const uint32_t fb = bar(s, B_VFULL0 + vr.slot);
-      mbar_arrive_expect_tx(fb, split ? static_cast<uint32_t>(nb * bk) * 128u * kBoxes : stage_bytes);
+      const uint32_t tx = split ? static_cast<uint32_t>(nb * bk) * 128u * kBoxes : stage_bytes;
+      mbar_arrive_expect_tx(fb, tx);
       const uint32_t dst = s.v + vr.slot * stage_bytes;
       if (!split) {
         if (WSATTN_BOUNDS(p.status, nb >= 1 && nb <= G && row >= y0 && row + nb * bk <= y0 + p.n)) {
 #pragma unroll
-          for (int c = 0; c < kBoxes; ++c) tma_load_2d(dst + c * box_pitch, &p.tm_v, fb, c * 64, row);
+          for (int c = 0; c < kBoxes; ++c)
+            tma_load_2d(dst + c * box_pitch, &p.tm_v, fb, c * 64, row);
         }
       } else {
         for (int i = 0; i < nb; ++i) {
@@ -859,11 +865,11 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
       uint64_t la = f2_pack(0.f, 0.f), lb = la;
       for (int j = 0; j < t.nstep; ++j) {
         int nblk;
-        const int kb = st.next(G, nblk);
+        const int pos = st.next(G, nblk);  // walk position of the step's first block
         const int keys = nblk * bk;
         int f16, n16;  // this warpgroup's 16-column chunks of the step
         wg_share(keys / 16, wg, f16, n16);
-        const uint32_t vis = kMasked ? chunk_vis(own, st, kb, f16, n16, bk / 16) : ~0u;
+        const uint32_t vis = kMasked ? chunk_vis(own, st, pos, f16, n16, bk / 16) : ~0u;
         const uint32_t c0 = static_cast<uint32_t>(16 * f16);  // first S column
         const uint32_t pb = pr.slot;
         // the S columns read and the P columns written lie in the allocation
@@ -905,11 +911,11 @@ __device__ void softmax_wg(const FwdParams& p, const Shared& s, uint32_t tbase) 
       }
       for (int j = 0; j < t.nstep; ++j) {
         int nblk;
-        const int kb = st.next(G, nblk);
+        const int pos = st.next(G, nblk);  // walk position of the step's first block
         const int keys = nblk * bk;
         int f16, n16;
         wg_share(keys / 16, wg, f16, n16);
-        const uint32_t vis = kMasked ? chunk_vis(own, st, kb, f16, n16, bk / 16) : ~0u;
+        const uint32_t vis = kMasked ? chunk_vis(own, st, pos, f16, n16, bk / 16) : ~0u;
         const uint32_t c0 = static_cast<uint32_t>(16 * f16);
         const bool cols_ok = WSATTN_BOUNDS(
             p.status, tc_.s + c0 + 16u * MAXC <= kTmemCols && n16 <= MAXC &&
