@@ -44,7 +44,7 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0}
 # ncu capture, keyed by workload; valid only for the kernel source it was
 # measured on (sha256 of forward.cu, first 16 hex digits).
 FORWARD_TRAFFIC = {
-    ("sr", 80, "8c6ff21246d9400e"): 1.4755e9,
+    ("sr", 80, "4cec5456289a3107"): 1.4867e9,
 }
 
 
