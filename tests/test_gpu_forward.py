@@ -76,6 +76,15 @@ def test_forward_full_size_sampled_parity(name):
     _whole_output_properties(wl, out, v)
 
 
+def test_sr_every_row():
+    # the headline workload in full: all 549,120 rows of the 24 heads against
+    # the fp64 oracle (about 30 s of oracle time on 16 cores)
+    wl = workload("sr")
+    q, k, v = generate(wl)
+    _, out, _ = gpu_run(wl, q, k, v)
+    _full_compare(wl, q, k, v, out)
+
+
 def test_fallback_heads_take_online_path_and_paths_agree():
     # SR-long: heads 5 and 17 are ineligible (bound above tau) and run the
     # online max; forcing either path on every head gives the same result.
