@@ -415,10 +415,12 @@ def run_gpu(args, wl, world, rank, local):
         e_end.record(s_comp)
 
     # untimed warm-up: the first transfers from freshly pinned host memory
-    # are slow (tens of ms over the first steps)
+    # are slow (tens of ms over the first steps), so at least 10 steps
+    # whatever --warmup says (with 3, a 20-step run measured 3.7 ms per step
+    # against 2.4 once past them)
     w0, w1 = torch.cuda.Event(), torch.cuda.Event()
     w0.record(s_comp)
-    e2e_run(max(3, args.warmup), w0, w1)
+    e2e_run(max(10, args.warmup), w0, w1)
     torch.cuda.synchronize()
     e_begin = torch.cuda.Event(enable_timing=True)
     e_end = torch.cuda.Event(enable_timing=True)
